@@ -1,0 +1,190 @@
+/*
+ * moe_decode.h -- C ABI of libmoe_decode.so, an output-centric ("warp decode")
+ * small-batch mixture-of-experts decode layer for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (the warp-decode post, cursor.com/blog/warp-decode, sections
+ * "The classic MoE path" and "How the two kernels work"):
+ *
+ *   for every token t and routed slot j (e = topk_ids[t,j]) and neuron i:
+ *     g = sum_K dq(W_gateup[e, i,   K]) * x[t,K]
+ *     u = sum_K dq(W_gateup[e, I+i, K]) * x[t,K]
+ *     h[t,j,i] = bf16( SiLU(g) * u )                     (moe_gate_up)
+ *   for every token t and output dimension r:
+ *     y[t,r] = bf16( sum_j topk_w[t,j] * sum_i dq(W_down[e_j, r, i]) * h[t,j,i] )
+ *                                                        (moe_down)
+ *
+ * dq() is MXFP8 dequantisation: one E4M3 code per element and one UE8M0
+ * exponent per 32 consecutive elements along the reduction axis (the block
+ * format named in the GC-MoE summary, onedev.kr/papers/1690, "How it is
+ * used"): dq = E4M3(code) * 2^(scale - 127). Dot products accumulate in FP32;
+ * h and y are rounded to BF16 (round to nearest even).
+ *
+ * Conventions shared by every call:
+ *   - Tensors are row-major and contiguous. bf16 tensors are passed as
+ *     uint16_t bit patterns. Device pointers are marked "device".
+ *   - Weights are borrowed: the handle keeps the pointers, never copies, and
+ *     the caller keeps them alive and unchanged until moe_decode_destroy.
+ *   - Compute calls only enqueue work on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and return at once. Argument errors are detected
+ *     on the host, return a non-zero status and enqueue nothing.
+ *   - T = 0 is a successful no-op. T may exceed 32: the library then works
+ *     through the tokens 32 at a time (expert dedup applies within a group).
+ *   - An expert id outside [0, E) contributes nothing (its h slice is zero)
+ *     and sets MOE_DEVICE_BAD_ID in the handle's device error word, read with
+ *     moe_decode_get_error. Nothing traps and nothing spins.
+ *   - Duplicate ids in a token's row are legal; their contributions add.
+ *   - Results are bitwise reproducible run to run (no atomics on data).
+ *   - Calls on one handle may run concurrently on different streams: the
+ *     handle holds no per-call device state except the error word (and the
+ *     staging buffers of moe_decode_forward_host, which serialises itself).
+ */
+#ifndef MOE_DECODE_H
+#define MOE_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,       /* null pointer, negative size, T > max_T ... */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2, /* H or I not a multiple of 32, k > 32, E > 1024 ... */
+  MOE_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment stated below */
+  MOE_ERR_CUDA = 4,              /* a CUDA runtime call failed */
+  MOE_ERR_DEVICE_FAULT = 5       /* moe_decode_get_error found a latched device flag */
+} moe_status_t;
+
+/* Bits of the device error word. */
+#define MOE_DEVICE_BAD_ID 0x1u     /* some topk_id was outside [0, E) */
+
+/* Flags of moe_decode_config_t. */
+#define MOE_FLAG_NO_PDL 0x1u       /* launch without programmatic dependent launch */
+
+typedef struct {
+  int32_t E;      /* experts, 1..1024 */
+  int32_t k;      /* routed experts per token, 1..min(E, 32) */
+  int32_t H;      /* hidden size, multiple of 32 */
+  int32_t I;      /* intermediate size per expert, multiple of 32 */
+  int32_t max_T;  /* largest T any call will pass (sizes host-side checks and
+                     the staging buffers of moe_decode_forward_host) */
+  uint32_t flags; /* MOE_FLAG_* */
+} moe_decode_config_t;
+
+typedef struct moe_decode* moe_decode_t;
+
+/*
+ * Create a handle for one layer on the current CUDA device.
+ *   w_gateup  device uint8 [E, 2I, H]   E4M3 codes; rows [0,I) gate, [I,2I) up
+ *   s_gateup  device uint8 [E, 2I, H/32] UE8M0 scale codes
+ *   w_down    device uint8 [E, H, I]    E4M3 codes
+ *   s_down    device uint8 [E, H, I/32] UE8M0 scale codes
+ * w_gateup and w_down must be 32-byte aligned (rows are then 32-byte aligned
+ * too); the scale arrays need no alignment. Allocates a 4-byte device error
+ * word (and, when max_T > 0, the staging buffers of
+ * moe_decode_forward_host). *out receives the handle; on error *out is NULL.
+ */
+moe_status_t moe_decode_create(const moe_decode_config_t* cfg,
+                               const uint8_t* w_gateup, const uint8_t* s_gateup,
+                               const uint8_t* w_down, const uint8_t* s_down,
+                               moe_decode_t* out);
+
+/* Release the handle and its device allocations (not the weights). NULL is a no-op. */
+moe_status_t moe_decode_destroy(moe_decode_t handle);
+
+/*
+ * Router: softmax over the E logits of each token, keep the k largest
+ * (ties to the lower expert id, ids in decreasing weight order), renormalise
+ * the kept weights to sum to one. The warp-decode post ("The classic MoE
+ * path") routes each token to k of E experts; the renormalisation follows the
+ * usual top-k router.
+ *   logits    device float [T, E]  (4-byte aligned)
+ *   topk_ids  device int32 [T, k]  out
+ *   topk_w    device float [T, k]  out
+ * Weights are computed in FP32 as exp(l_j - l_max) / sum over the kept j.
+ */
+moe_status_t moe_route(moe_decode_t handle, int32_t T, const float* logits,
+                       int32_t* topk_ids, float* topk_w, void* stream);
+
+/*
+ * Per-step expert dedup schedule, exactly as the kernels build it (exported
+ * for inspection; the kernels rebuild it on chip and never read this).
+ * For T <= 32 tokens:
+ *   uniq     device int32 [min(E, T*k)]    ascending unique valid expert ids
+ *   offsets  device int32 [min(E, T*k)+1]  pairs of uniq[u] are pairs[offsets[u]:offsets[u+1]]
+ *   pairs    device int32 [T*k]            flattened slots p = t*k + j, ascending within an expert
+ *   n_uniq   device int32 [1]              number of unique experts
+ * Entries past n_uniq / offsets[n_uniq] are left unchanged.
+ */
+moe_status_t moe_dedup_schedule(moe_decode_t handle, int32_t T, const int32_t* topk_ids,
+                                int32_t* uniq, int32_t* offsets, int32_t* pairs,
+                                int32_t* n_uniq, void* stream);
+
+/*
+ * Gate/up projection (kernel moe_gate_up_3d_batched; the warp-decode post,
+ * "How the two kernels work", first two paragraphs). Each unique expert's
+ * gate and up rows are streamed once per group of tokens and serve every
+ * token routed to it.
+ *   x         device bf16 [T, H]     32-byte aligned
+ *   topk_ids  device int32 [T, k]
+ *   h         device bf16 [T, k, I]  out, 32-byte aligned
+ */
+moe_status_t moe_gate_up(moe_decode_t handle, int32_t T, const uint16_t* x,
+                         const int32_t* topk_ids, uint16_t* h, void* stream);
+
+/*
+ * Down projection with the routing-weighted sum over the top-k experts
+ * (kernel moe_down_3d_batched; the warp-decode post, "How the two kernels
+ * work", third paragraph onward). One warp owns one output y[t, r].
+ *   h         device bf16 [T, k, I]  32-byte aligned
+ *   topk_ids  device int32 [T, k]
+ *   topk_w    device float [T, k]
+ *   y         device bf16 [T, H]     out
+ */
+moe_status_t moe_down(moe_decode_t handle, int32_t T, const uint16_t* h,
+                      const int32_t* topk_ids, const float* topk_w, uint16_t* y,
+                      void* stream);
+
+/*
+ * The whole layer: moe_gate_up then moe_down on one stream. The down kernel
+ * is launched as a programmatic dependent of the gate/up kernel and fetches
+ * its weight rows (which depend only on topk_ids) while the gate/up kernel
+ * drains; topk_ids and topk_w must therefore be complete before this call's
+ * work starts on `stream`, which stream order guarantees. h is the caller's
+ * [T, k, I] bf16 buffer (32-byte aligned).
+ */
+moe_status_t moe_decode_layer(moe_decode_t handle, int32_t T, const uint16_t* x,
+                              const int32_t* topk_ids, const float* topk_w,
+                              uint16_t* h, uint16_t* y, void* stream);
+
+/*
+ * The whole layer from and to HOST memory: copies x, topk_ids and topk_w to
+ * the handle's device staging buffers, runs moe_decode_layer, copies y back
+ * and waits for the stream. Host buffers should be pinned (cudaHostAlloc or
+ * torch pin_memory) for asynchronous copies. T <= max_T. Calls on one handle
+ * must not overlap (they share the staging buffers).
+ *   x_host [T,H] bf16, ids_host [T,k] int32, w_host [T,k] float, y_host [T,H] bf16 out
+ */
+moe_status_t moe_decode_forward_host(moe_decode_t handle, int32_t T, const uint16_t* x_host,
+                                     const int32_t* ids_host, const float* w_host,
+                                     uint16_t* y_host, void* stream);
+
+/*
+ * Wait for the device, read and clear the device error word. *device_flags
+ * receives the MOE_DEVICE_* bits seen since the last call; the return value
+ * is MOE_ERR_DEVICE_FAULT when any bit was set, MOE_OK otherwise.
+ */
+moe_status_t moe_decode_get_error(moe_decode_t handle, uint32_t* device_flags);
+
+/* Static, human-readable name of a status. */
+const char* moe_status_string(moe_status_t status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t moe_decode_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_DECODE_H */

@@ -106,6 +106,17 @@ def dedup_schedule(ids: np.ndarray, E: int):
             np.array(pairs, dtype=np.int32))
 
 
+def _slots_by_expert(ids: np.ndarray, E: int, tokens) -> dict[int, list[tuple[int, int]]]:
+    T, k = ids.shape
+    by_e: dict[int, list[tuple[int, int]]] = {}
+    for t in (range(T) if tokens is None else tokens):
+        for j in range(k):
+            e = int(ids[t, j])
+            if 0 <= e < E:
+                by_e.setdefault(e, []).append((t, j))
+    return by_e
+
+
 def gate_up(x: np.ndarray, ids: np.ndarray, experts: ExpertSource, E: int, I: int,
             tokens=None) -> tuple[np.ndarray, np.ndarray]:
     """h[t, j, :] = SiLU(dq(Wg_e) x_t) * (dq(Wu_e) x_t), e = ids[t, j].
@@ -113,24 +124,20 @@ def gate_up(x: np.ndarray, ids: np.ndarray, experts: ExpertSource, E: int, I: in
     x: float64 [T, H] holding the bf16 input values exactly.
     Returns (h_spec, h_pure), float64 [T, k, I]; h_spec is rounded to bf16.
     `tokens` restricts the work to a subset of tokens (other rows stay zero).
+    Each expert is dequantised once and released after its slots are done.
     """
     x = np.asarray(x, dtype=np.float64)
     ids = np.asarray(ids)
     T, k = ids.shape
     h_pure = np.zeros((T, k, I), dtype=np.float64)
-    deq: dict[int, np.ndarray] = {}
-    for t in (range(T) if tokens is None else tokens):
-        for j in range(k):
-            e = int(ids[t, j])
-            if not 0 <= e < E:
-                continue
-            if e not in deq:
-                wgu, sgu = _get(experts, e)[:2]
-                deq[e] = dequantize(wgu, sgu)
-            W = deq[e]
+    for e, slots in _slots_by_expert(ids, E, tokens).items():
+        wgu, sgu = _get(experts, e)[:2]
+        W = dequantize(wgu, sgu)
+        for t, j in slots:
             gate = W[:I] @ x[t]
             up = W[I:] @ x[t]
             h_pure[t, j] = silu(gate) * up
+        del W
     return bf16_rne(h_pure), h_pure
 
 
@@ -146,18 +153,14 @@ def down(h: np.ndarray, ids: np.ndarray, w: np.ndarray, experts: ExpertSource, E
     wt = np.asarray(w, dtype=np.float32).astype(np.float64)
     T, k = ids.shape
     rows = np.arange(H) if rows is None else np.asarray(rows)
-    y = np.zeros((T, len(rows)), dtype=np.float64)
-    deq: dict[int, np.ndarray] = {}
-    for t in (range(T) if tokens is None else tokens):
-        for j in range(k):
-            e = int(ids[t, j])
-            if not 0 <= e < E:
-                continue
-            if e not in deq:
-                wd, sd = _get(experts, e)[2:4]
-                deq[e] = dequantize(wd[rows], sd[rows])
-            y[t] += wt[t, j] * (deq[e] @ h[t, j])
-    return y
+    terms = np.zeros((T, k, len(rows)), dtype=np.float64)
+    for e, slots in _slots_by_expert(ids, E, tokens).items():
+        wd, sd = _get(experts, e)[2:4]
+        W = dequantize(wd[rows], sd[rows])
+        for t, j in slots:
+            terms[t, j] = wt[t, j] * (W @ h[t, j])
+        del W
+    return terms.sum(axis=1)
 
 
 def layer(x, ids, w, experts: ExpertSource, E: int, H: int, I: int, tokens=None, rows=None):

@@ -1,0 +1,352 @@
+// Host side of the C ABI declared in include/moe_decode.h: argument checks,
+// handle lifetime, launch configuration and the programmatic-dependent-launch
+// chaining of the two projection kernels.
+#include "moe_decode.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+#include <new>
+
+#include "moe_kernels.cuh"
+
+namespace {
+
+constexpr int kMaxE = 1024;  // the schedule's expert bitmap is 32 words
+constexpr int kMaxK = 32;    // a token's slots are bits of one 32-bit mask
+constexpr int kVersion = 100;
+// h[t] (k*I FP32 values) is staged in shared memory by the down kernel
+constexpr size_t kMaxDownSmem = 200 * 1024;
+
+}  // namespace
+
+struct moe_decode {
+  moe_decode_config_t cfg;
+  const uint8_t* wgu;
+  const uint8_t* sgu;
+  const uint8_t* wd;
+  const uint8_t* sd;
+  int device;
+  int num_sms;
+  int gate_up_ctas_per_sm;
+  size_t down_smem;
+  uint32_t* d_err;
+  // staging buffers of moe_decode_forward_host (max_T tokens)
+  uint16_t* d_x;
+  int32_t* d_ids;
+  float* d_w;
+  uint16_t* d_h;
+  uint16_t* d_y;
+};
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+template <typename Kernel, typename... Args>
+cudaError_t launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                   Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+bool use_pdl(const moe_decode* m) { return (m->cfg.flags & MOE_FLAG_NO_PDL) == 0; }
+
+// ---- gate/up ---------------------------------------------------------------
+
+template <int NT, int KMAX>
+cudaError_t launch_gate_up_t(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
+  const long long units_max = (long long)std::min(p.E, p.T * p.k) * p.I;
+  const long long ctas_needed = (units_max + moe::kWarps - 1) / moe::kWarps;
+  const long long cap = (long long)m->num_sms * m->gate_up_ctas_per_sm;
+  const int grid = (int)std::max(1LL, std::min(ctas_needed, cap));
+  return launch(moe::moe_gate_up_3d_batched<NT, KMAX>, dim3(grid), dim3(moe::kThreads), 0, s,
+                use_pdl(m), p);
+}
+
+template <int KMAX>
+cudaError_t launch_gate_up_k(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
+  if (p.T <= 1) return launch_gate_up_t<1, KMAX>(m, p, s);
+  if (p.T <= 2) return launch_gate_up_t<2, KMAX>(m, p, s);
+  if (p.T <= 4) return launch_gate_up_t<4, KMAX>(m, p, s);
+  return launch_gate_up_t<8, KMAX>(m, p, s);
+}
+
+cudaError_t launch_gate_up(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
+  if (p.k <= 8) return launch_gate_up_k<8>(m, p, s);
+  return launch_gate_up_k<32>(m, p, s);
+}
+
+// ---- down ------------------------------------------------------------------
+
+constexpr int kDownQ = 8;
+
+cudaError_t launch_down(const moe_decode* m, const moe::DownParams& p, cudaStream_t s) {
+  return launch(moe::moe_down_3d_batched<kDownQ>, dim3(p.H / moe::kWarps, p.T),
+                dim3(moe::kThreads), m->down_smem, s, use_pdl(m), p);
+}
+
+// ---- per-call token chunking -----------------------------------------------
+
+moe_status_t gate_up_chunks(moe_decode* m, int T, const uint16_t* x, const int32_t* ids,
+                            uint16_t* h, cudaStream_t s) {
+  const moe_decode_config_t& c = m->cfg;
+  for (int t0 = 0; t0 < T; t0 += moe::kMaxTokensPerLaunch) {
+    moe::GateUpParams p;
+    p.T = std::min(moe::kMaxTokensPerLaunch, T - t0);
+    p.x = x + (size_t)t0 * c.H;
+    p.ids = ids + (size_t)t0 * c.k;
+    p.h = h + (size_t)t0 * c.k * c.I;
+    p.wgu = m->wgu;
+    p.sgu = m->sgu;
+    p.err = m->d_err;
+    p.k = c.k;
+    p.E = c.E;
+    p.H = c.H;
+    p.I = c.I;
+    if (launch_gate_up(m, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status_t down_chunks(moe_decode* m, int T, const uint16_t* h, const int32_t* ids,
+                         const float* w, uint16_t* y, bool early, cudaStream_t s) {
+  const moe_decode_config_t& c = m->cfg;
+  for (int t0 = 0; t0 < T; t0 += moe::kMaxTokensPerLaunch) {
+    moe::DownParams p;
+    p.T = std::min(moe::kMaxTokensPerLaunch, T - t0);
+    p.h = h + (size_t)t0 * c.k * c.I;
+    p.ids = ids + (size_t)t0 * c.k;
+    p.w = w + (size_t)t0 * c.k;
+    p.y = y + (size_t)t0 * c.H;
+    p.wd = m->wd;
+    p.sd = m->sd;
+    p.err = m->d_err;
+    p.k = c.k;
+    p.E = c.E;
+    p.H = c.H;
+    p.I = c.I;
+    p.early = early ? 1 : 0;
+    if (launch_down(m, p, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status_t check_T(const moe_decode* m, int32_t T) {
+  if (!m) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > m->cfg.max_T) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+void free_all(moe_decode* m) {
+  if (!m) return;
+  cudaFree(m->d_err);
+  cudaFree(m->d_x);
+  cudaFree(m->d_ids);
+  cudaFree(m->d_w);
+  cudaFree(m->d_h);
+  cudaFree(m->d_y);
+  delete m;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_decode_create(const moe_decode_config_t* cfg, const uint8_t* w_gateup,
+                               const uint8_t* s_gateup, const uint8_t* w_down,
+                               const uint8_t* s_down, moe_decode_t* out) {
+  if (out) *out = nullptr;
+  if (!cfg || !out || !w_gateup || !s_gateup || !w_down || !s_down) return MOE_ERR_INVALID_ARG;
+  const moe_decode_config_t c = *cfg;
+  if (c.E < 1 || c.k < 1 || c.H < 1 || c.I < 1 || c.max_T < 0) return MOE_ERR_INVALID_ARG;
+  if (c.k > c.E) return MOE_ERR_INVALID_ARG;
+  if (c.E > kMaxE || c.k > kMaxK || c.H % 32 || c.I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((c.flags & ~MOE_FLAG_NO_PDL) != 0) return MOE_ERR_INVALID_ARG;
+  const size_t down_smem = (size_t)c.k * c.I * sizeof(float);
+  if (down_smem > kMaxDownSmem) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(w_gateup, 32) || !aligned(w_down, 32)) return MOE_ERR_MISALIGNED;
+
+  moe_decode* m = new (std::nothrow) moe_decode();
+  if (!m) return MOE_ERR_CUDA;
+  m->cfg = c;
+  m->wgu = w_gateup;
+  m->sgu = s_gateup;
+  m->wd = w_down;
+  m->sd = s_down;
+  m->down_smem = down_smem;
+  bool ok = cudaGetDevice(&m->device) == cudaSuccess &&
+            cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) ==
+                cudaSuccess &&
+            cudaMalloc(&m->d_err, sizeof(uint32_t)) == cudaSuccess &&
+            cudaMemset(m->d_err, 0, sizeof(uint32_t)) == cudaSuccess;
+  // a per-function limit shared by every handle: always the library's maximum
+  ok = ok && cudaFuncSetAttribute(moe::moe_down_3d_batched<kDownQ>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kMaxDownSmem) == cudaSuccess;
+  int occ = 0;
+  ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                 &occ, moe::moe_gate_up_3d_batched<1, 8>, moe::kThreads, 0) == cudaSuccess;
+  m->gate_up_ctas_per_sm = std::max(1, occ);
+  if (ok && c.max_T > 0) {
+    const size_t T = (size_t)c.max_T;
+    ok = cudaMalloc(&m->d_x, T * c.H * 2) == cudaSuccess &&
+         cudaMalloc(&m->d_ids, T * c.k * 4) == cudaSuccess &&
+         cudaMalloc(&m->d_w, T * c.k * 4) == cudaSuccess &&
+         cudaMalloc(&m->d_h, T * c.k * c.I * 2) == cudaSuccess &&
+         cudaMalloc(&m->d_y, T * c.H * 2) == cudaSuccess;
+  }
+  if (!ok) {
+    free_all(m);
+    return MOE_ERR_CUDA;
+  }
+  *out = m;
+  return MOE_OK;
+}
+
+moe_status_t moe_decode_destroy(moe_decode_t m) {
+  if (!m) return MOE_OK;
+  free_all(m);
+  return MOE_OK;
+}
+
+moe_status_t moe_route(moe_decode_t m, int32_t T, const float* logits, int32_t* topk_ids,
+                       float* topk_w, void* stream) {
+  moe_status_t st = check_T(m, T);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4)) return MOE_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const dim3 grid((T + moe::kWarps - 1) / moe::kWarps), block(moe::kThreads);
+  const int E = m->cfg.E, k = m->cfg.k;
+  cudaError_t e;
+  if (E <= 128)
+    e = launch(moe::moe_route_topk<4>, grid, block, 0, s, use_pdl(m), logits, T, E, k, topk_ids, topk_w);
+  else if (E <= 256)
+    e = launch(moe::moe_route_topk<8>, grid, block, 0, s, use_pdl(m), logits, T, E, k, topk_ids, topk_w);
+  else
+    e = launch(moe::moe_route_topk<32>, grid, block, 0, s, use_pdl(m), logits, T, E, k, topk_ids, topk_w);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_dedup_schedule(moe_decode_t m, int32_t T, const int32_t* topk_ids, int32_t* uniq,
+                                int32_t* offsets, int32_t* pairs, int32_t* n_uniq, void* stream) {
+  moe_status_t st = check_T(m, T);
+  if (st != MOE_OK) return st;
+  if (T > moe::kMaxTokensPerLaunch) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!topk_ids || !uniq || !offsets || !pairs || !n_uniq) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int E = m->cfg.E, k = m->cfg.k;
+  cudaError_t e;
+  if (k <= 8)
+    e = launch(moe::moe_dedup_schedule_kernel<8>, dim3(1), dim3(32), 0, s, use_pdl(m), topk_ids, T,
+               k, E, uniq, offsets, pairs, n_uniq, m->d_err);
+  else
+    e = launch(moe::moe_dedup_schedule_kernel<32>, dim3(1), dim3(32), 0, s, use_pdl(m), topk_ids,
+               T, k, E, uniq, offsets, pairs, n_uniq, m->d_err);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_gate_up(moe_decode_t m, int32_t T, const uint16_t* x, const int32_t* topk_ids,
+                         uint16_t* h, void* stream) {
+  moe_status_t st = check_T(m, T);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!x || !topk_ids || !h) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 32) || !aligned(h, 32) || !aligned(topk_ids, 4)) return MOE_ERR_MISALIGNED;
+  return gate_up_chunks(m, T, x, topk_ids, h, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_down(moe_decode_t m, int32_t T, const uint16_t* h, const int32_t* topk_ids,
+                      const float* topk_w, uint16_t* y, void* stream) {
+  moe_status_t st = check_T(m, T);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!h || !topk_ids || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(h, 32) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(y, 2))
+    return MOE_ERR_MISALIGNED;
+  return down_chunks(m, T, h, topk_ids, topk_w, y, false, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_decode_layer(moe_decode_t m, int32_t T, const uint16_t* x,
+                              const int32_t* topk_ids, const float* topk_w, uint16_t* h,
+                              uint16_t* y, void* stream) {
+  moe_status_t st = check_T(m, T);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!x || !topk_ids || !topk_w || !h || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 32) || !aligned(h, 32) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) ||
+      !aligned(y, 2))
+    return MOE_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T <= moe::kMaxTokensPerLaunch) {
+    st = gate_up_chunks(m, T, x, topk_ids, h, s);
+    if (st != MOE_OK) return st;
+    return down_chunks(m, T, h, topk_ids, topk_w, y, use_pdl(m), s);
+  }
+  // several token groups: finish every gate/up launch before the downs so the
+  // early weight fetch of a down never precedes a gate/up it does not follow
+  st = gate_up_chunks(m, T, x, topk_ids, h, s);
+  if (st != MOE_OK) return st;
+  return down_chunks(m, T, h, topk_ids, topk_w, y, false, s);
+}
+
+moe_status_t moe_decode_forward_host(moe_decode_t m, int32_t T, const uint16_t* x_host,
+                                     const int32_t* ids_host, const float* w_host,
+                                     uint16_t* y_host, void* stream) {
+  moe_status_t st = check_T(m, T);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !ids_host || !w_host || !y_host) return MOE_ERR_INVALID_ARG;
+  const moe_decode_config_t& c = m->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(m->d_x, x_host, (size_t)T * c.H * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(m->d_ids, ids_host, (size_t)T * c.k * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(m->d_w, w_host, (size_t)T * c.k * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = moe_decode_layer(m, T, m->d_x, m->d_ids, m->d_w, m->d_h, m->d_y, stream);
+  if (st != MOE_OK) return st;
+  if (cudaMemcpyAsync(y_host, m->d_y, (size_t)T * c.H * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t moe_decode_get_error(moe_decode_t m, uint32_t* device_flags) {
+  if (!m || !device_flags) return MOE_ERR_INVALID_ARG;
+  uint32_t v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(&v, m->d_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(m->d_err, 0, sizeof(v)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *device_flags = v;
+  return v ? MOE_ERR_DEVICE_FAULT : MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_MISALIGNED: return "misaligned pointer";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_FAULT: return "device flagged an error";
+  }
+  return "unknown status";
+}
+
+int32_t moe_decode_version(void) { return kVersion; }
+
+}  // extern "C"

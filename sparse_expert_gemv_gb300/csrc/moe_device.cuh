@@ -1,0 +1,186 @@
+// Device building blocks shared by the decode-layer kernels: PTX wrappers for
+// streaming loads, MXFP8 element/scale decode, bf16 handling, warp reductions,
+// programmatic-dependent-launch controls and the per-warp expert dedup
+// schedule.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr uint32_t kDeviceBadId = 0x1u;
+
+// ---------------------------------------------------------------------------
+// loads
+// ---------------------------------------------------------------------------
+
+// 32 bytes of a weight row that is read once per step: no L1 allocation, and
+// an L2 eviction-first hint so the stream does not push activations out.
+__device__ __forceinline__ void ld_weights32(const uint8_t* p, uint32_t (&r)[8]) {
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "l"(p));
+}
+
+// 16 bytes of activations that many warps re-read: keep them in L1 and L2.
+__device__ __forceinline__ uint4 ld_act16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::evict_last.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_scale(const uint8_t* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// MXFP8 decode
+// ---------------------------------------------------------------------------
+
+// Four E4M3 codes (byte n = element n) to FP32. The hardware conversion to
+// f16 is exact for every finite E4M3 value (f16 covers 2^-14..65504 with 10
+// mantissa bits; E4M3 spans 2^-9..448 with 3), and f16 -> f32 is exact.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t q, float& f0, float& f1, float& f2,
+                                              float& f3) {
+  uint32_t lo, hi;
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(q));
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(f0), "=f"(f1)
+      : "r"(lo));
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(f2), "=f"(f3)
+      : "r"(hi));
+}
+
+// UE8M0 scale code s -> 2^(s-127) as FP32, built from its bit pattern:
+// exponent field s for s >= 1, the subnormal 2^-127 for s = 0, NaN for 0xFF.
+__device__ __forceinline__ float ue8m0_to_f32(uint32_t s) {
+  uint32_t bits = s << 23;
+  bits = (s == 0u) ? 0x00400000u : bits;
+  bits = (s == 255u) ? 0x7fc00000u : bits;
+  return __uint_as_float(bits);
+}
+
+// ---------------------------------------------------------------------------
+// bf16
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// FP32 -> bf16 bits, round to nearest even (NaN stays NaN).
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// warp reductions (the butterfly of the warp-decode post, "How the two
+// kernels work": shfl.sync.bfly, no shared memory, no barrier)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// Block until the grids this one depends on have completed and their memory
+// is visible. A no-op when the kernel was not launched as a dependent.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid on the stream to start launching its blocks.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// ---------------------------------------------------------------------------
+// Per-warp expert dedup schedule for up to 32 tokens.
+//
+// Lane t holds token t's k expert ids. The set of routed experts is a bitmap
+// over E (word w held by lane w, E <= 1024); its popcount prefix numbers the
+// unique experts in ascending id order. For a given expert, each lane reports
+// which of its slots j route there (jmask), and a ballot gives the tokens.
+// Everything lives in registers plus 32 words of per-warp shared memory, so
+// each warp builds it alone with no block barrier.
+// ---------------------------------------------------------------------------
+
+template <int KMAX>
+struct WarpSchedule {
+  int id[KMAX];      // this lane's token's ids (-1: slot unused or invalid)
+  uint32_t badmask;  // slots j of this lane's token whose id is outside [0, E)
+  uint32_t word;     // routed-expert bitmap word `lane`
+  int excl;          // unique experts in words below `lane`
+  int n_unique;
+
+  __device__ __forceinline__ void build(const int32_t* __restrict__ ids, int T, int k, int E,
+                                        uint32_t* sm_words, uint32_t* err) {
+    const int lane = threadIdx.x & 31;
+    badmask = 0u;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      int v = -1;
+      if (lane < T && j < k) {
+        v = __ldg(ids + lane * k + j);
+        if (v < 0 || v >= E) {
+          badmask |= 1u << j;
+          v = -1;
+        }
+      }
+      id[j] = v;
+    }
+    if (badmask) atomicOr(err, kDeviceBadId);
+    sm_words[lane] = 0u;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (id[j] >= 0) atomicOr(&sm_words[id[j] >> 5], 1u << (id[j] & 31));
+    __syncwarp();
+    word = sm_words[lane];
+    __syncwarp();
+    const int cnt = __popc(word);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += v;
+    }
+    excl = incl - cnt;
+    n_unique = __shfl_sync(kFull, incl, 31);
+  }
+
+  // Expert id of the u-th unique expert (ascending), 0 <= u < n_unique.
+  __device__ __forceinline__ int expert(int u) const {
+    const int lane = threadIdx.x & 31;
+    const unsigned owner = __ballot_sync(kFull, u >= excl && u < excl + __popc(word));
+    const int L = __ffs(owner) - 1;
+    const uint32_t w = __shfl_sync(kFull, word, L);
+    const int n = u - __shfl_sync(kFull, excl, L);     // n-th set bit of w (0-based)
+    const bool mine = ((w >> lane) & 1u) && (__popc(w & ((1u << lane) - 1u)) == n);
+    return L * 32 + (__ffs(__ballot_sync(kFull, mine)) - 1);
+  }
+
+  // Bits j of this lane's token whose id equals e.
+  __device__ __forceinline__ uint32_t jmask(int e) const {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) m |= (id[j] == e ? 1u : 0u) << j;
+    return m;
+  }
+};
+
+}  // namespace moe

@@ -1,0 +1,408 @@
+// The decode-layer kernels: router, dedup-schedule export, gate/up, down.
+//
+// Output-centric throughout (the warp-decode post, cursor.com/blog/warp-decode,
+// "What we changed" and "How the two kernels work"): every warp owns output
+// scalars, streams the weight rows they need straight from HBM, decodes MXFP8
+// to FP32 in registers, accumulates in private registers and finishes with a
+// shfl.xor butterfly. No warp shares partial sums with another.
+#pragma once
+
+#include "moe_device.cuh"
+
+namespace moe {
+
+constexpr int kWarps = 8;               // 8-warp CTAs, as in the pages' gate/up kernel
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxTokensPerLaunch = 32; // tokens of one schedule (one per lane)
+
+// ---------------------------------------------------------------------------
+// Router: softmax over E logits, top-k (ties to the lower id), renormalise.
+// One warp per token; lane l holds logits l, l+32, ...
+// ---------------------------------------------------------------------------
+
+template <int RMAX>
+__global__ void __launch_bounds__(kThreads) moe_route_topk(const float* __restrict__ logits, int T,
+                                                           int E, int k, int32_t* __restrict__ ids,
+                                                           float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_trigger();
+  if (t >= T) return;
+  float v[RMAX];
+  const float* row = logits + (size_t)t * E;
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r) {
+    const int e = lane + 32 * r;
+    v[r] = (e < E) ? __ldg(row + e) : 0.f;
+  }
+  uint32_t taken = 0;
+  float my_v = 0.f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float best = -__int_as_float(0x7f800000);
+    int bidx = 0x7fffffff;
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      const int e = lane + 32 * r;
+      if (e < E && !((taken >> r) & 1u) && (v[r] > best || (v[r] == best && e < bidx))) {
+        best = v[r];
+        bidx = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, best, o);
+      const int oi = __shfl_xor_sync(kFull, bidx, o);
+      if (ov > best || (ov == best && oi < bidx)) {
+        best = ov;
+        bidx = oi;
+      }
+    }
+    if ((bidx & 31) == lane) taken |= 1u << (bidx >> 5);
+    if (lane == j) {
+      my_v = best;
+      my_id = bidx;
+    }
+  }
+  const float top = __shfl_sync(kFull, my_v, 0);
+  const float ex = (lane < k) ? expf(my_v - top) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+  if (lane < k) {
+    ids[(size_t)t * k + lane] = my_id;
+    w[(size_t)t * k + lane] = ex / sum;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Dedup schedule export (one warp, <= 32 tokens): the same WarpSchedule the
+// projection kernels build on chip, written out for inspection.
+// ---------------------------------------------------------------------------
+
+template <int KMAX>
+__global__ void __launch_bounds__(32) moe_dedup_schedule_kernel(const int32_t* __restrict__ ids,
+                                                                int T, int k, int E,
+                                                                int32_t* uniq, int32_t* offsets,
+                                                                int32_t* pairs, int32_t* n_uniq,
+                                                                uint32_t* err) {
+  __shared__ uint32_t sm_words[32];
+  const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
+  WarpSchedule<KMAX> s;
+  s.build(ids, T, k, E, sm_words, err);
+  int base = 0;
+  for (int u = 0; u < s.n_unique; ++u) {
+    const int e = s.expert(u);
+    const uint32_t jm = s.jmask(e);
+    const int cnt = __popc(jm);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int pos = base + incl - cnt;
+    for (uint32_t m = jm; m; m &= m - 1) pairs[pos++] = lane * k + (__ffs(m) - 1);
+    if (lane == 0) {
+      uniq[u] = e;
+      offsets[u] = base;
+    }
+    base += __shfl_sync(kFull, incl, 31);
+  }
+  if (lane == 0) {
+    offsets[s.n_unique] = base;
+    *n_uniq = s.n_unique;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Gate/up: h[t, j, i] = bf16(SiLU(g) * u) for every token routed to expert e.
+//
+// Work unit = (unique expert u, neuron i): one warp streams gate row i and up
+// row i of expert u once and applies them to up to NT of the expert's tokens
+// at a time (more tokens: another pass over the same rows, from L2). Lane l
+// takes the 32-element blocks b = l, l+32, ... of the H-long rows, so each
+// 256-bit load of a warp covers 1 KB of one row. The block's partial dots are
+// scaled by the block's UE8M0 factor and accumulated in FP32 per token.
+// ---------------------------------------------------------------------------
+
+struct GateUpParams {
+  const uint16_t* x;      // [T, H] bf16
+  const int32_t* ids;     // [T, k]
+  const uint8_t* wgu;     // [E, 2I, H]
+  const uint8_t* sgu;     // [E, 2I, H/32]
+  uint16_t* h;            // [T, k, I] bf16
+  uint32_t* err;
+  int T, k, E, H, I;
+};
+
+template <int NT>
+__device__ __forceinline__ void gate_up_block(const uint32_t (&qg)[8], const uint32_t (&qu)[8],
+                                              float scg, float scu, const uint16_t* __restrict__ x,
+                                              const int (&tok)[NT], int nt, int H, int b,
+                                              float (&ag)[NT], float (&au)[NT]) {
+  float pg[NT], pu[NT];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) pg[n] = pu[n] = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float g[8], u[8];
+    e4m3x4_to_f32(qg[2 * c], g[0], g[1], g[2], g[3]);
+    e4m3x4_to_f32(qg[2 * c + 1], g[4], g[5], g[6], g[7]);
+    e4m3x4_to_f32(qu[2 * c], u[0], u[1], u[2], u[3]);
+    e4m3x4_to_f32(qu[2 * c + 1], u[4], u[5], u[6], u[7]);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      if (n < nt) {
+        const uint4 xv = ld_act16(x + (size_t)tok[n] * H + b * 32 + c * 8);
+        const float xs[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
+                             bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          pg[n] = fmaf(g[m], xs[m], pg[n]);
+          pu[n] = fmaf(u[m], xs[m], pu[n]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    ag[n] = fmaf(pg[n], scg, ag[n]);
+    au[n] = fmaf(pu[n], scu, au[n]);
+  }
+}
+
+template <int NT, int KMAX>
+__global__ void __launch_bounds__(kThreads, 2) moe_gate_up_3d_batched(GateUpParams p) {
+  __shared__ uint32_t sm_words[kWarps][32];
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  pdl_wait();      // x and topk_ids come from upstream work
+  pdl_trigger();   // the down kernel may start fetching its weights
+  WarpSchedule<KMAX> s;
+  s.build(p.ids, p.T, p.k, p.E, sm_words[wid], p.err);
+  const int H = p.H, I = p.I, nb = H >> 5;
+  // A slot with an out-of-range id gets no unit; its h slice is defined as zero.
+  if (__any_sync(kFull, s.badmask != 0u)) {
+    for (int t = blockIdx.x * kWarps + wid; t < p.T; t += gridDim.x * kWarps) {
+      const uint32_t bm = __shfl_sync(kFull, s.badmask, t);
+      for (uint32_t m = bm; m; m &= m - 1) {
+        uint16_t* row = p.h + ((size_t)t * p.k + (__ffs(m) - 1)) * I;
+        for (int i = lane; i < I; i += 32) row[i] = 0;
+      }
+    }
+  }
+  const long long units = (long long)s.n_unique * I;
+  for (long long unit = (long long)blockIdx.x * kWarps + wid; unit < units;
+       unit += (long long)gridDim.x * kWarps) {
+    const int u = (int)(unit / I);
+    const int i = (int)(unit - (long long)u * I);
+    const int e = s.expert(u);
+    const uint32_t jm = s.jmask(e);
+    uint32_t tokens = __ballot_sync(kFull, jm != 0u);
+    const size_t row = (size_t)e * 2 * I + i;
+    const uint8_t* wg = p.wgu + row * H;
+    const uint8_t* wu = wg + (size_t)I * H;
+    const uint8_t* sg = p.sgu + row * nb;
+    const uint8_t* su = sg + (size_t)I * nb;
+    while (tokens) {
+      int tok[NT];
+      int nt = 0;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        tok[n] = tokens ? __ffs(tokens) - 1 : 0;
+        if (tokens) {
+          tokens &= tokens - 1;
+          ++nt;
+        }
+      }
+      float ag[NT], au[NT];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
+      // two blocks in flight per lane: issue block b+32 before computing b
+      uint32_t qg0[8], qu0[8], qg1[8], qu1[8];
+      uint32_t s0g = 0, s0u = 0, s1g = 0, s1u = 0;
+      int b = lane;
+      if (b < nb) {
+        ld_weights32(wg + b * 32, qg0);
+        ld_weights32(wu + b * 32, qu0);
+        s0g = ld_scale(sg + b);
+        s0u = ld_scale(su + b);
+      }
+      while (b < nb) {
+        const int b1 = b + 32;
+        if (b1 < nb) {
+          ld_weights32(wg + b1 * 32, qg1);
+          ld_weights32(wu + b1 * 32, qu1);
+          s1g = ld_scale(sg + b1);
+          s1u = ld_scale(su + b1);
+        }
+        gate_up_block<NT>(qg0, qu0, ue8m0_to_f32(s0g), ue8m0_to_f32(s0u), p.x, tok, nt, H, b, ag,
+                          au);
+        if (b1 >= nb) break;
+        const int b2 = b1 + 32;
+        if (b2 < nb) {
+          ld_weights32(wg + b2 * 32, qg0);
+          ld_weights32(wu + b2 * 32, qu0);
+          s0g = ld_scale(sg + b2);
+          s0u = ld_scale(su + b2);
+        }
+        gate_up_block<NT>(qg1, qu1, ue8m0_to_f32(s1g), ue8m0_to_f32(s1u), p.x, tok, nt, H, b1, ag,
+                          au);
+        b = b2;
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        if (n < nt) {
+          const float g = warp_sum(ag[n]);
+          const float up = warp_sum(au[n]);
+          const uint32_t jt = __shfl_sync(kFull, jm, tok[n]);
+          const float hv = (g / (1.0f + expf(-g))) * up;
+          const uint16_t hb = f32_to_bf16_rn(hv);
+          if (lane < p.k && ((jt >> lane) & 1u)) p.h[((size_t)tok[n] * p.k + lane) * I + i] = hb;
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Down: y[t, r] = bf16(sum_j w[t, j] * sum_i dq(Wd[e_j, r, i]) * h[t, j, i]).
+//
+// One warp per (token t, output row r); a CTA covers 8 consecutive rows of one
+// token. The warp's k rows Wd[e_j, r, :] are laid out as k*I/32 blocks of 32
+// elements and dealt to the lanes (block f = j*I/32 + b to lane f % 32), so all
+// 32 lanes stream even when I/32 < 32. h[t] (k*I bf16) is read once per CTA
+// into shared memory as FP32, 16-byte chunks XOR-swizzled by block index so
+// that lanes reading consecutive blocks hit distinct banks. The routing weight
+// multiplies each block's scaled partial inside the single FP32 accumulator.
+// With `early` set, the first round of weight loads is issued before waiting
+// for the gate/up kernel (those rows depend only on topk_ids).
+// ---------------------------------------------------------------------------
+
+struct DownParams {
+  const uint16_t* h;      // [T, k, I] bf16
+  const int32_t* ids;     // [T, k]
+  const float* w;         // [T, k]
+  const uint8_t* wd;      // [E, H, I]
+  const uint8_t* sd;      // [E, H, I/32]
+  uint16_t* y;            // [T, H] bf16
+  uint32_t* err;
+  int T, k, E, H, I;
+  int early;
+};
+
+template <int QMAX>
+__device__ __forceinline__ void down_load_round(const DownParams& p, int f0, int nf, int nbI, int r,
+                                                int id, float wj, uint32_t (&q)[QMAX][8],
+                                                float (&sc)[QMAX], float (&wsel)[QMAX],
+                                                bool (&valid)[QMAX]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int qi = 0; qi < QMAX; ++qi) {
+    const int f = f0 + lane + 32 * qi;
+    const int j = (f < nf) ? f / nbI : 0;
+    const int b = f - j * nbI;
+    const int e = __shfl_sync(kFull, id, j);
+    wsel[qi] = __shfl_sync(kFull, wj, j);
+    valid[qi] = (f < nf) && (e >= 0);
+    if (valid[qi]) {
+      const size_t rowi = (size_t)e * p.H + r;
+      ld_weights32(p.wd + rowi * p.I + b * 32, q[qi]);
+      sc[qi] = ue8m0_to_f32(ld_scale(p.sd + rowi * nbI + b));
+    } else {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) q[qi][m] = 0u;
+      sc[qi] = 0.f;
+    }
+  }
+}
+
+template <int QMAX>
+__device__ __forceinline__ float down_compute_round(const float4* __restrict__ sh, int f0,
+                                                    const uint32_t (&q)[QMAX][8],
+                                                    const float (&sc)[QMAX],
+                                                    const float (&wsel)[QMAX],
+                                                    const bool (&valid)[QMAX], float acc) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int qi = 0; qi < QMAX; ++qi) {
+    if (valid[qi]) {
+      const int blk = f0 + lane + 32 * qi;
+      const float4* hb = sh + (size_t)blk * 8;
+      const int sw = blk & 7;
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float wv[8];
+        e4m3x4_to_f32(q[qi][2 * c], wv[0], wv[1], wv[2], wv[3]);
+        e4m3x4_to_f32(q[qi][2 * c + 1], wv[4], wv[5], wv[6], wv[7]);
+        const float4 h0 = hb[(2 * c) ^ sw];
+        const float4 h1 = hb[(2 * c + 1) ^ sw];
+        a0 = fmaf(wv[0], h0.x, a0);
+        a1 = fmaf(wv[1], h0.y, a1);
+        a0 = fmaf(wv[2], h0.z, a0);
+        a1 = fmaf(wv[3], h0.w, a1);
+        a0 = fmaf(wv[4], h1.x, a0);
+        a1 = fmaf(wv[5], h1.y, a1);
+        a0 = fmaf(wv[6], h1.z, a0);
+        a1 = fmaf(wv[7], h1.w, a1);
+      }
+      acc = fmaf((a0 + a1) * sc[qi], wsel[qi], acc);
+    }
+  }
+  return acc;
+}
+
+template <int QMAX>
+__global__ void __launch_bounds__(kThreads, 2) moe_down_3d_batched(DownParams p) {
+  extern __shared__ float4 sh_h[];   // [k*I/32 blocks][8 chunks] FP32, swizzled
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  const int t = blockIdx.y;
+  const int r = blockIdx.x * kWarps + wid;
+  const int k = p.k, I = p.I, nbI = I >> 5, nf = k * nbI;
+  if (!p.early) pdl_wait();
+  int id = -1;
+  float wj = 0.f;
+  if (lane < k) {
+    id = __ldg(p.ids + (size_t)t * k + lane);
+    wj = __ldg(p.w + (size_t)t * k + lane);
+    if (id < 0 || id >= p.E) {
+      if (blockIdx.x == 0 && wid == 0) atomicOr(p.err, kDeviceBadId);
+      id = -1;
+    }
+  }
+  uint32_t q[QMAX][8];
+  float sc[QMAX], wsel[QMAX];
+  bool valid[QMAX];
+  down_load_round<QMAX>(p, 0, nf, nbI, r, id, wj, q, sc, wsel, valid);
+  if (p.early) pdl_wait();   // h is written by the gate/up kernel
+  {
+    const uint16_t* ht = p.h + (size_t)t * k * I;
+    const int nchunk = (k * I) >> 3;   // 8 bf16 per 16-byte load
+    for (int c = threadIdx.x; c < nchunk; c += kThreads) {
+      const uint4 v = *reinterpret_cast<const uint4*>(ht + (size_t)c * 8);
+      const int blk = c >> 2;
+      const int ch = (2 * c) & 7;
+      const int sw = blk & 7;
+      sh_h[blk * 8 + (ch ^ sw)] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+      sh_h[blk * 8 + ((ch + 1) ^ sw)] =
+          make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+    }
+  }
+  __syncthreads();
+  pdl_trigger();
+  float acc = down_compute_round<QMAX>(sh_h, 0, q, sc, wsel, valid, 0.f);
+  for (int f0 = 32 * QMAX; f0 < nf; f0 += 32 * QMAX) {
+    down_load_round<QMAX>(p, f0, nf, nbI, r, id, wj, q, sc, wsel, valid);
+    acc = down_compute_round<QMAX>(sh_h, f0, q, sc, wsel, valid, acc);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) p.y[(size_t)t * p.H + r] = f32_to_bf16_rn(acc);
+}
+
+}  // namespace moe

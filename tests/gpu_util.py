@@ -1,0 +1,85 @@
+"""Helpers for the GPU parity tests: device copies of seeded layers, tolerances."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as wl
+
+
+def bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def tensor_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def device_weights(w: wl.Workload, experts: dict, device, fill_code=wl.NAN_CODE):
+    """Full [E, ...] device tensors; experts absent from `experts` hold NaN codes
+    (a kernel that reads them poisons exactly the outputs that used them)."""
+    E, H, I = w.E, w.H, w.I
+    wgu = torch.full((E, 2 * I, H), fill_code, dtype=torch.uint8, device=device)
+    sgu = torch.full((E, 2 * I, H // 32), 127, dtype=torch.uint8, device=device)
+    wd = torch.full((E, H, I), fill_code, dtype=torch.uint8, device=device)
+    sd = torch.full((E, H, I // 32), 127, dtype=torch.uint8, device=device)
+    for e, (a, b, c, d) in experts.items():
+        wgu[e].copy_(torch.from_numpy(a))
+        sgu[e].copy_(torch.from_numpy(b))
+        wd[e].copy_(torch.from_numpy(c))
+        sd[e].copy_(torch.from_numpy(d))
+    return wgu, sgu, wd, sd
+
+
+def tol_y(ref: np.ndarray) -> np.ndarray:
+    """|y - y_ref| <= 2^-7 |y_ref| + 1e-3 rms(y_ref)."""
+    rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    return 2.0 ** -7 * np.abs(ref) + 1e-3 * rms
+
+
+def tol_h(ref: np.ndarray) -> np.ndarray:
+    """|h - h_spec| <= 2^-8 |h_spec| + 1e-3 rms(h_spec): one bf16 step at a rounding boundary."""
+    rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    return 2.0 ** -8 * np.abs(ref) + 1e-3 * rms
+
+
+def assert_within(got: np.ndarray, ref: np.ndarray, tol: np.ndarray, what: str) -> dict:
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite outputs"
+    err = np.abs(got - ref)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())}/{bad.size} outside tolerance, "
+                           f"worst {float(err.max()):.3e} at {np.unravel_index(err.argmax(), err.shape)}")
+    return metrics(got, ref)
+
+
+def metrics(got: np.ndarray, ref: np.ndarray) -> dict:
+    g, r = got.ravel(), ref.ravel()
+    nr = float(np.linalg.norm(r))
+    cos = float(g @ r / (np.linalg.norm(g) * nr)) if nr > 0 else 1.0
+    return {"rel_l2": float(np.linalg.norm(g - r) / nr) if nr > 0 else 0.0,
+            "cosine": cos, "max_abs": float(np.abs(g - r).max()) if g.size else 0.0}
+
+
+class Case:
+    """A seeded workload with its routing and the experts it needs."""
+
+    def __init__(self, c: int, T: int | None = None, tokens=None):
+        self.w = w = wl.workload(c)
+        self.seed = wl.seed_of(c)
+        self.T = w.T if T is None else T
+        self.x_bits = wl.make_x(w, self.seed, self.T)
+        self.logits = wl.make_logits(w, self.seed, self.T)
+        self.ids, self.tw = oracle.route(self.logits, w.k)
+        self.tokens = list(range(self.T)) if tokens is None else list(tokens)
+        need = np.unique(self.ids[self.tokens])
+        self.experts = wl.make_experts(w, self.seed, need)
+
+    def x64(self):
+        return wl.bf16_bits_to_f64(self.x_bits)
+
+    def ref(self):
+        w = self.w
+        return oracle.layer(self.x64(), self.ids, self.tw, self.experts, w.E, w.H, w.I,
+                            tokens=self.tokens)

@@ -1,0 +1,205 @@
+"""GPU edge cases: empty and ragged shapes, duplicates, invalid ids, extreme
+scales, one-hot inputs, invariants, determinism, graphs and the host path."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_util import (assert_within, bf16_tensor, device_weights, tensor_to_f64, tol_h, tol_y)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+class Small:
+    """A small synthetic layer with every expert generated."""
+
+    def __init__(self, dev, E, k, H, I, T, seed=7, sigma=0.05, flags=0):
+        from sparse_expert_gemv_gb300 import MoEDecode
+        self.w = wl.Workload(90, "edge", E, k, H, I, T, sigma)
+        self.seed = seed
+        self.experts = wl.make_experts(self.w, seed, range(E))
+        self.wts = device_weights(self.w, self.experts, dev)
+        self.layer = MoEDecode(*self.wts, k=k, max_T=max(T, 1), flags=flags)
+        self.dev = dev
+        self.x_bits = wl.make_x(self.w, seed, T)
+        self.ids, self.tw = oracle.route(wl.make_logits(self.w, seed, T), k)
+
+    def run(self, x_bits=None, ids=None, tw=None):
+        x_bits = self.x_bits if x_bits is None else x_bits
+        ids = self.ids if ids is None else ids
+        tw = self.tw if tw is None else tw
+        x = bf16_tensor(x_bits, self.dev)
+        di = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).to(self.dev)
+        dw = torch.from_numpy(np.ascontiguousarray(tw, dtype=np.float32)).to(self.dev)
+        h = self.layer.gate_up(x, di)
+        y = self.layer.down(h, di, dw)
+        torch.cuda.synchronize()
+        return h, y
+
+    def ref(self, x_bits=None, ids=None, tw=None):
+        x_bits = self.x_bits if x_bits is None else x_bits
+        ids = self.ids if ids is None else ids
+        tw = self.tw if tw is None else tw
+        w = self.w
+        return oracle.layer(wl.bf16_bits_to_f64(x_bits), ids, tw, self.experts, w.E, w.H, w.I)
+
+    def check(self, **kw):
+        h, y = self.run(**kw)
+        r = self.ref(**kw)
+        assert_within(tensor_to_f64(h), r["h_spec"], tol_h(r["h_spec"]), "h")
+        assert_within(tensor_to_f64(y), r["y_spec"], tol_y(r["y_spec"]), "y")
+        return h, y
+
+
+@pytest.mark.parametrize("E,k,H,I,T", [
+    (5, 3, 1184, 96, 5),      # H/32 = 37 blocks: ragged lanes; I/32 = 3; k odd; T < NT
+    (16, 16, 64, 64, 3),      # k > 8 (wide slot masks)
+    (8, 2, 256, 128, 37),     # T > 32: two token groups
+    (3, 1, 32, 32, 1),        # smallest shapes
+    (64, 8, 2048, 32, 6),     # I = 32: one block per row
+    (4, 4, 96, 160, 33),      # every expert shared by many tokens, 2 groups
+])
+def test_ragged_shapes(dev, E, k, H, I, T):
+    Small(dev, E, k, H, I, T).check()
+
+
+def test_T_zero_is_a_noop(dev):
+    s = Small(dev, 8, 2, 256, 128, 1)
+    x = torch.zeros((0, 256), dtype=torch.bfloat16, device=dev)
+    ids = torch.zeros((0, 2), dtype=torch.int32, device=dev)
+    h = s.layer.gate_up(x, ids)
+    y = s.layer.down(h, ids, torch.zeros((0, 2), dtype=torch.float32, device=dev))
+    assert h.numel() == 0 and y.numel() == 0
+
+
+def test_duplicate_ids_add_up(dev):
+    s = Small(dev, 6, 4, 256, 64, 4)
+    ids = s.ids.copy()
+    ids[0, 1] = ids[0, 0]
+    ids[2, :] = ids[2, 0]
+    s.check(ids=ids)
+
+
+def test_out_of_range_id_contributes_nothing(dev):
+    s = Small(dev, 6, 3, 256, 64, 3)
+    ids = s.ids.copy()
+    ids[1, 2] = 6
+    ids[2, 0] = -4
+    h, y = s.check(ids=ids)
+    hb = tensor_to_f64(h)
+    assert np.all(hb[1, 2] == 0) and np.all(hb[2, 0] == 0)
+    from sparse_expert_gemv_gb300 import MOE_DEVICE_BAD_ID
+    assert s.layer.get_error() == MOE_DEVICE_BAD_ID
+    assert s.layer.get_error() == 0      # reading clears it
+
+
+def test_one_hot_x_selects_weight_columns(dev):
+    s = Small(dev, 4, 2, 2048, 64, 4)
+    for c in [0, 31, 32, 1023, 1024, 2047]:
+        xb = np.zeros((4, 2048), dtype=np.float32)
+        xb[:, c] = 1.0
+        bits = torch.from_numpy(xb).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        h, _ = s.run(x_bits=bits)
+        r = s.ref(x_bits=bits)
+        # each dot has one product (exact in FP32): only SiLU's FP32 rounding differs
+        assert_within(tensor_to_f64(h), r["h_spec"], 2.0 ** -8 * np.abs(r["h_spec"]) + 1e-30, "h")
+
+
+def test_extreme_scales_bitwise_through_down(dev):
+    # one expert whose down rows r carry (code, scale) pairs at block 1 and a
+    # one-hot h selecting column 40 (block 1, element 8): y[r] = bf16(E4M3 * 2^(s-127)),
+    # a single product, exact in FP32 unless it overflows (then inf on both sides)
+    from sparse_expert_gemv_gb300 import MoEDecode
+    E, k, H, I = 1, 1, 64, 64
+    pairs = [(0x01, 0), (0x7E, 0), (0x38, 0), (0x08, 1), (0x7E, 254), (0x38, 254), (0xB8, 200),
+             (0x01, 100), (0x00, 254), (0x07, 5), (0xFE, 130), (0x3C, 127)]
+    wd = np.zeros((H, I), np.uint8)
+    sd = np.full((H, I // 32), 127, np.uint8)
+    for r, (c, s) in enumerate(pairs):
+        wd[r, 40] = c
+        sd[r, 1] = s
+    experts = {0: (np.zeros((2 * I, H), np.uint8), np.full((2 * I, H // 32), 127, np.uint8), wd, sd)}
+    wts = device_weights(wl.Workload(91, "x", E, k, H, I, 1, 0.0), experts, dev)
+    layer = MoEDecode(*wts, k=1, max_T=1)
+    h = torch.zeros((1, 1, I), dtype=torch.bfloat16, device=dev)
+    h[0, 0, 40] = 1.0
+    y = layer.down(h, torch.zeros((1, 1), dtype=torch.int32, device=dev),
+                   torch.ones((1, 1), dtype=torch.float32, device=dev))
+    torch.cuda.synchronize()
+    got = tensor_to_f64(y)[0]
+    want = oracle.bf16_rne(oracle.dequantize(wd, sd)[:, 40])
+    assert np.array_equal(got[:len(pairs)], want[:len(pairs)]), (got[:len(pairs)], want[:len(pairs)])
+
+
+def test_zero_routing_weight_and_topk_order(dev):
+    s = Small(dev, 8, 4, 512, 96, 5)
+    tw = s.tw.copy()
+    tw[:, 2] = 0
+    s.check(tw=tw)
+    perm = [3, 1, 0, 2]
+    _, y1 = s.run()
+    _, y2 = s.run(ids=s.ids[:, perm], tw=s.tw[:, perm])
+    ref = s.ref()["y_spec"]
+    assert_within(tensor_to_f64(y2), tensor_to_f64(y1), tol_y(ref), "y permuted top-k")
+
+
+def test_bitwise_deterministic_and_graph_capture(dev):
+    s = Small(dev, 16, 4, 1024, 256, 8)
+    h1, y1 = s.run()
+    h2, y2 = s.run()
+    assert torch.equal(h1.view(torch.int16), h2.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    x = bf16_tensor(s.x_bits, dev)
+    ids = torch.from_numpy(s.ids).to(dev)
+    tw = torch.from_numpy(s.tw).to(dev)
+    h = torch.empty_like(h1)
+    y = torch.empty_like(y1)
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        s.layer.layer(x, ids, tw, h=h, y=y)       # warm up outside capture
+    torch.cuda.current_stream().wait_stream(st)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    y.zero_()
+    with torch.cuda.graph(g):
+        s.layer.layer(x, ids, tw, h=h, y=y)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y1.view(torch.int16))
+
+
+def test_no_pdl_flag_and_host_path(dev):
+    from sparse_expert_gemv_gb300 import MOE_FLAG_NO_PDL
+    a = Small(dev, 8, 4, 512, 128, 6)
+    b = Small(dev, 8, 4, 512, 128, 6, flags=MOE_FLAG_NO_PDL)
+    _, ya = a.run()
+    _, yb = b.run()
+    assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
+    x = torch.from_numpy(a.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ids = torch.from_numpy(a.ids).pin_memory()
+    tw = torch.from_numpy(a.tw).pin_memory()
+    yh = a.layer.forward_host(x, ids, tw)
+    assert torch.equal(yh.view(torch.int16), ya.cpu().view(torch.int16))
+
+
+def test_bad_arguments_raise(dev):
+    from sparse_expert_gemv_gb300 import MoEError
+    s = Small(dev, 8, 2, 256, 128, 2)
+    x = bf16_tensor(s.x_bits, dev)
+    ids = torch.from_numpy(s.ids).to(dev)
+    big = torch.zeros((3, 256), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(MoEError):
+        s.layer.gate_up(big, torch.zeros((3, 2), dtype=torch.int32, device=dev))   # T > max_T
+    mis = torch.zeros(2 * 256 + 8, dtype=torch.bfloat16, device=dev)[8:].view(2, 256)
+    with pytest.raises(MoEError):
+        s.layer.gate_up(mis, ids)                                                  # 16-byte offset
