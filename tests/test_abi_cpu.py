@@ -13,9 +13,11 @@ HEADER = os.path.join(ROOT, "include", "moe_decode.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from sparse_expert_gemv_gb300 import build as b
-    if not os.path.exists(b.OUT) or os.path.getmtime(b.OUT) < max(
-            os.path.getmtime(os.path.join(b.HERE, "csrc", f)) for f in os.listdir(os.path.join(b.HERE, "csrc"))):
+    import __graft_entry__
+    b = __graft_entry__._build_module()
+    csrc = os.path.join(b.HERE, "csrc")
+    newest = max(os.path.getmtime(os.path.join(csrc, f)) for f in os.listdir(csrc))
+    if not os.path.exists(b.OUT) or os.path.getmtime(b.OUT) < newest:
         b.build()
     from sparse_expert_gemv_gb300 import _lib
     return _lib.lib

