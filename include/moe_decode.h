@@ -183,6 +183,39 @@ const char* moe_status_string(moe_status_t status);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t moe_decode_version(void);
 
+/*
+ * The whole layer without any device allocation. The pages have no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc, such as code that runs inside another framework's memory
+ * pool, plugin enqueue functions that must not allocate, or real-time loops
+ * where an allocation may block. It takes no handle (creating one allocates)
+ * and keeps the intermediate h, plus an internal error word, in one
+ * fixed-size array in the library's static device memory, which every GPU
+ * that loads the library holds until the process exits.
+ *
+ *   cfg, w_gateup, s_gateup, w_down, s_down   as for moe_decode_create
+ *                                              (cfg->max_T is ignored)
+ *   x, topk_ids, topk_w, y                     as for moe_decode_layer
+ *
+ * T * k * I * 2 bytes of h must fit in MOE_NOALLOC_SCRATCH_BYTES (1 MiB,
+ * e.g. T = 32 tokens at k = 8, I = 2048); a larger call returns
+ * MOE_ERR_UNSUPPORTED_SHAPE and enqueues nothing. The first call on a device
+ * looks up the array's device address and sets the kernels' attributes for
+ * that device; make that first call before any stream capture. All calls on
+ * a device share the one array and it keeps the previous call's contents
+ * (nothing in it needs to start at zero: every h value the down kernel reads
+ * is written earlier in the same call), so calls whose work overlaps on the
+ * GPU, for example on two streams, race and corrupt each other's h.
+ * Out-of-range expert ids still contribute nothing, but this call has no way
+ * to report them.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+moe_status_t moe_decode_layer_noalloc(const moe_decode_config_t* cfg,
+                                      const uint8_t* w_gateup, const uint8_t* s_gateup,
+                                      const uint8_t* w_down, const uint8_t* s_down, int32_t T,
+                                      const uint16_t* x, const int32_t* topk_ids,
+                                      const float* topk_w, uint16_t* y, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_decode.so")
 MOE_OK = 0
 MOE_DEVICE_BAD_ID = 0x1
 MOE_FLAG_NO_PDL = 0x1
+MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 STATUS_NAMES = {
     0: "MOE_OK",
@@ -55,6 +56,8 @@ SIGNATURES = {
     "moe_decode_get_error": (_st, [_p, ctypes.POINTER(ctypes.c_uint32)]),
     "moe_status_string": (ctypes.c_char_p, [_st]),
     "moe_decode_version": (_i32, []),
+    "moe_decode_layer_noalloc": (_st, [ctypes.POINTER(MoEConfig), _p, _p, _p, _p, _i32, _p, _p, _p,
+                                       _p, _p]),
 }
 
 

@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <new>
 
 #include "moe_kernels.cuh"
@@ -350,3 +351,98 @@ const char* moe_status_string(moe_status_t status) {
 int32_t moe_decode_version(void) { return kVersion; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// The layer without device allocation (moe_decode_layer_noalloc).
+//
+// For callers that cannot call cudaMalloc: h and the error word live in one
+// file-scope array of static device memory. In host code the array's name is
+// only a stand-in for the device object, so its device address is looked up
+// with cudaGetSymbolAddress once per device (with that device current) and
+// that address is what the kernels receive.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr size_t kNoAllocHBytes = MOE_NOALLOC_SCRATCH_BYTES;
+constexpr int kNoAllocMaxDevices = 64;
+
+// [0, kNoAllocHBytes): h of the current call; then the 4-byte error word.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocHBytes + 256];
+
+struct NoAllocDevice {
+  bool ready;
+  uint8_t* scratch;   // device address of g_noalloc_scratch on this device
+  int num_sms;
+  int gate_up_ctas_per_sm;
+};
+
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// One-time set-up for the current device: the array's device address, the
+// SM count, the gate/up occupancy and the down kernel's shared-memory limit.
+moe_status_t noalloc_device(int dev, NoAllocDevice* out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return MOE_ERR_CUDA;
+    int occ = 0;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(moe::moe_down_3d_batched<kDownQ>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kMaxDownSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, moe::moe_gate_up_3d_batched<1, 8>,
+                                                      moe::kThreads, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    d.scratch = static_cast<uint8_t*>(ptr);
+    d.gate_up_ctas_per_sm = std::max(1, occ);
+    d.ready = true;
+  }
+  *out = d;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_decode_layer_noalloc(const moe_decode_config_t* cfg,
+                                                 const uint8_t* w_gateup, const uint8_t* s_gateup,
+                                                 const uint8_t* w_down, const uint8_t* s_down,
+                                                 int32_t T, const uint16_t* x,
+                                                 const int32_t* topk_ids, const float* topk_w,
+                                                 uint16_t* y, void* stream) {
+  if (!cfg || !w_gateup || !s_gateup || !w_down || !s_down) return MOE_ERR_INVALID_ARG;
+  const moe_decode_config_t c = *cfg;
+  if (c.E < 1 || c.k < 1 || c.H < 1 || c.I < 1 || T < 0) return MOE_ERR_INVALID_ARG;
+  if (c.k > c.E) return MOE_ERR_INVALID_ARG;
+  if (c.E > kMaxE || c.k > kMaxK || c.H % 32 || c.I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((c.flags & ~MOE_FLAG_NO_PDL) != 0) return MOE_ERR_INVALID_ARG;
+  if ((size_t)c.k * c.I * sizeof(float) > kMaxDownSmem) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((size_t)T * c.k * c.I * 2 > kNoAllocHBytes) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(w_gateup, 32) || !aligned(w_down, 32)) return MOE_ERR_MISALIGNED;
+  if (T == 0) return MOE_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  NoAllocDevice d;
+  const moe_status_t st = noalloc_device(dev, &d);
+  if (st != MOE_OK) return st;
+  // a handle on the stack: every device pointer in it is either the caller's
+  // or inside the static array, and its staging buffers stay null
+  moe_decode m = {};
+  m.cfg = c;
+  m.cfg.max_T = T;
+  m.wgu = w_gateup;
+  m.sgu = s_gateup;
+  m.wd = w_down;
+  m.sd = s_down;
+  m.device = dev;
+  m.num_sms = d.num_sms;
+  m.gate_up_ctas_per_sm = d.gate_up_ctas_per_sm;
+  m.down_smem = (size_t)c.k * c.I * sizeof(float);
+  m.d_err = reinterpret_cast<uint32_t*>(d.scratch + kNoAllocHBytes);
+  return moe_decode_layer(&m, T, x, topk_ids, topk_w, reinterpret_cast<uint16_t*>(d.scratch), y,
+                          stream);
+}
