@@ -39,9 +39,15 @@ def tol_y(ref: np.ndarray) -> np.ndarray:
 
 
 def tol_h(ref: np.ndarray) -> np.ndarray:
-    """|h - h_spec| <= 2^-8 |h_spec| + 1e-3 rms(h_spec): one bf16 step at a rounding boundary."""
+    """|h - h_spec| <= 2^-7 |h_spec| + 1e-3 rms(h_spec).
+
+    h is stored in bf16 (8 significant bits). When the GPU's FP32 value and the
+    oracle's float64 value fall on opposite sides of a rounding midpoint, the
+    two bf16 results are one step apart, and one step is at most 2^-7 of the
+    value (at the bottom of a binade).
+    """
     rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
-    return 2.0 ** -8 * np.abs(ref) + 1e-3 * rms
+    return 2.0 ** -7 * np.abs(ref) + 1e-3 * rms
 
 
 def assert_within(got: np.ndarray, ref: np.ndarray, tol: np.ndarray, what: str) -> dict:

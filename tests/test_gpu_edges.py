@@ -110,7 +110,7 @@ def test_one_hot_x_selects_weight_columns(dev):
         h, _ = s.run(x_bits=bits)
         r = s.ref(x_bits=bits)
         # each dot has one product (exact in FP32): only SiLU's FP32 rounding differs
-        assert_within(tensor_to_f64(h), r["h_spec"], 2.0 ** -8 * np.abs(r["h_spec"]) + 1e-30, "h")
+        assert_within(tensor_to_f64(h), r["h_spec"], 2.0 ** -7 * np.abs(r["h_spec"]) + 1e-30, "h")
 
 
 def test_extreme_scales_bitwise_through_down(dev):
