@@ -3,6 +3,8 @@
 // chaining of the two projection kernels.
 #include "moe_decode.h"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -12,6 +14,7 @@
 #include <new>
 
 #include "moe_kernels.cuh"
+#include "moe_layer_fused.cuh"
 
 namespace {
 
@@ -33,7 +36,12 @@ struct moe_decode {
   int num_sms;
   int gate_up_ctas_per_sm;
   size_t down_smem;
-  uint32_t* d_err;
+  size_t smem_per_block;          // opt-in shared-memory maximum of one CTA
+  bool fused_ok;                  // the single-token fused kernel can run here
+  CUtensorMap tm_codes;           // W_gateup codes / scales as 2D tensors for its TMA
+  CUtensorMap tm_scales;
+  uint32_t* d_err;                // device error word (4 bytes) ...
+  unsigned long long* d_bar;      // ... and, 8 bytes on, the fused kernel's grid barrier
   // staging buffers of moe_decode_forward_host (max_T tokens)
   uint16_t* d_x;
   int32_t* d_ids;
@@ -96,6 +104,165 @@ constexpr int kDownQ = 8;
 cudaError_t launch_down(const moe_decode* m, const moe::DownParams& p, cudaStream_t s) {
   return launch(moe::moe_down_3d_batched<kDownQ>, dim3(p.H / moe::kWarps, p.T),
                 dim3(moe::kThreads), m->down_smem, s, use_pdl(m), p);
+}
+
+// ---- single-token fused layer ----------------------------------------------
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int gcd_int(int a, int b) { return b ? gcd_int(b, a % b) : a; }
+
+// Ring geometry of moe_layer_fused_t1 for this handle's shape; false when the
+// shape or the pointers do not suit it (the two-kernel path is used instead).
+bool plan_fused(const moe_decode* m, moe::FusedParams& fp, size_t& smem) {
+  const moe_decode_config_t& c = m->cfg;
+  if (!m->fused_ok || c.H % 512 || c.I % 128 || !aligned(m->sgu, 16) || !aligned(m->sd, 16))
+    return false;
+  const int KC = (c.H % 1024 == 0) ? 1024 : 512;       // one TMA box row is <= 1 KB
+  const size_t slot = round_up((size_t)33 * KC, 128);   // 2 x 16 rows of codes + scales
+  const int nbI = c.I / 32;
+  const int RG = 16 / gcd_int(16, nbI);
+  if (c.H % RG) return false;
+  const int rows_cta = (c.H / RG + m->num_sms - 1) / m->num_sms * RG;
+  int RC = std::min(rows_cta, moe::kFusedConsumers / RG * RG);
+  if (RC < RG) return false;
+  const size_t EB = round_up((size_t)RC * (c.I + nbI), 16);
+  const int GE = (int)std::min<size_t>(32, slot / EB);
+  if (GE < 1) return false;
+  const size_t fixed = (size_t)c.H * 4 + (size_t)c.k * c.I * 4 + (moe::kFusedConsumers + 1) * 128;
+  int S = 8;
+  while (S > 2 && (size_t)S * (slot + 16) + fixed > m->smem_per_block) --S;
+  smem = (size_t)S * (slot + 16) + fixed;
+  if (smem > m->smem_per_block) return false;
+  fp.KC = KC;
+  fp.S = S;
+  fp.slot_bytes = (int)slot;
+  fp.RG = RG;
+  fp.RC = RC;
+  fp.GE = GE;
+  fp.EB = (int)EB;
+  return true;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no link to libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A [rows, cols] uint32 matrix with a row pitch of `pitch` bytes, read in
+// boxes of box_rows x box_cols.
+bool encode_u32_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch,
+                   uint32_t box_cols, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The W_gateup tensor maps of the fused kernel (codes [E*2I, H/4] uint32,
+// scales [E*2I, H/128] uint32; boxes of 16 rows by KC codes / KC/32 scales).
+bool encode_fused_maps(moe_decode* m, int KC) {
+  const moe_decode_config_t& c = m->cfg;
+  const uint64_t rows = (uint64_t)c.E * 2 * c.I;
+  return encode_u32_2d(&m->tm_codes, m->wgu, c.H / 4, rows, c.H, KC / 4, moe::kFusedNeurons) &&
+         encode_u32_2d(&m->tm_scales, m->sgu, c.H / 128, rows, c.H / 32, KC / 128,
+                       moe::kFusedNeurons);
+}
+
+cudaError_t set_fused_attributes(size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(moe::moe_layer_fused_t1<8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(moe::moe_layer_fused_t1<32>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return e;
+}
+
+// One persistent CTA per SM; cooperative so that every CTA is resident for
+// the grid barrier between the two phases.
+cudaError_t launch_fused(const moe_decode* m, const moe::FusedParams& fp, size_t smem,
+                         cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(m->num_sms);
+  cfg.blockDim = dim3(moe::kFusedThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = use_pdl(m) ? 2 : 1;
+  if (fp.k <= 8) return cudaLaunchKernelEx(&cfg, moe::moe_layer_fused_t1<8>, fp);
+  return cudaLaunchKernelEx(&cfg, moe::moe_layer_fused_t1<32>, fp);
+}
+
+// Device limits shared by handles and the allocation-free call: SM count,
+// gate/up occupancy, shared memory, and whether the fused kernel fits one CTA
+// per SM (it then runs as a cooperative launch of num_sms CTAs).
+bool query_fused(moe_decode* m) {
+  int v_blk = 0, coop = 0;
+  if (cudaDeviceGetAttribute(&v_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device) != cudaSuccess)
+    return false;
+  m->smem_per_block = (size_t)v_blk;
+  m->fused_ok = false;
+  if (!coop || set_fused_attributes(m->smem_per_block) != cudaSuccess) return true;
+  moe::FusedParams fp = {};
+  size_t smem = 0;
+  m->fused_ok = true;
+  if (!plan_fused(m, fp, smem)) {
+    m->fused_ok = false;
+    return true;
+  }
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, moe::moe_layer_fused_t1<8>,
+                                                    moe::kFusedThreads, smem) != cudaSuccess)
+    return false;
+  m->fused_ok = occ >= 1 && encode_fused_maps(m, fp.KC);
+  return true;
+}
+
+moe_status_t fused_layer(moe_decode* m, const uint16_t* x, const int32_t* ids, const float* w,
+                         uint16_t* h, uint16_t* y, cudaStream_t s) {
+  moe::FusedParams fp = {};
+  size_t smem = 0;
+  plan_fused(m, fp, smem);
+  const moe_decode_config_t& c = m->cfg;
+  fp.x = x;
+  fp.ids = ids;
+  fp.w = w;
+  fp.wgu = m->wgu;
+  fp.sgu = m->sgu;
+  fp.wd = m->wd;
+  fp.sd = m->sd;
+  fp.h = h;
+  fp.y = y;
+  fp.err = m->d_err;
+  fp.grid_bar = m->d_bar;
+  fp.tm_codes = m->tm_codes;
+  fp.tm_scales = m->tm_scales;
+  fp.k = c.k;
+  fp.E = c.E;
+  fp.H = c.H;
+  fp.I = c.I;
+  return launch_fused(m, fp, smem, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 // ---- per-call token chunking -----------------------------------------------
@@ -190,8 +357,9 @@ moe_status_t moe_decode_create(const moe_decode_config_t* cfg, const uint8_t* w_
   bool ok = cudaGetDevice(&m->device) == cudaSuccess &&
             cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) ==
                 cudaSuccess &&
-            cudaMalloc(&m->d_err, sizeof(uint32_t)) == cudaSuccess &&
-            cudaMemset(m->d_err, 0, sizeof(uint32_t)) == cudaSuccess;
+            cudaMalloc(&m->d_err, 16) == cudaSuccess && cudaMemset(m->d_err, 0, 16) == cudaSuccess;
+  if (ok) m->d_bar = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(m->d_err) + 8);
+  ok = ok && query_fused(m);
   // a per-function limit shared by every handle: always the library's maximum
   ok = ok && cudaFuncSetAttribute(moe::moe_down_3d_batched<kDownQ>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -293,6 +461,7 @@ moe_status_t moe_decode_layer(moe_decode_t m, int32_t T, const uint16_t* x,
       !aligned(y, 2))
     return MOE_ERR_MISALIGNED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 1 && m->fused_ok) return fused_layer(m, x, topk_ids, topk_w, h, y, s);
   if (T <= moe::kMaxTokensPerLaunch) {
     st = gate_up_chunks(m, T, x, topk_ids, h, s);
     if (st != MOE_OK) return st;
@@ -330,7 +499,10 @@ moe_status_t moe_decode_get_error(moe_decode_t m, uint32_t* device_flags) {
   uint32_t v = 0;
   if (cudaDeviceSynchronize() != cudaSuccess ||
       cudaMemcpy(&v, m->d_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemset(m->d_err, 0, sizeof(v)) != cudaSuccess)
+      cudaMemset(m->d_err, 0, sizeof(v)) != cudaSuccess ||
+      // a wait that gave up may have left the grid barrier's count off a
+      // multiple of the grid size: start it again from zero
+      ((v & moe::kDeviceTimeout) && cudaMemset(m->d_bar, 0, 8) != cudaSuccess))
     return MOE_ERR_CUDA;
   *device_flags = v;
   return v ? MOE_ERR_DEVICE_FAULT : MOE_OK;
@@ -375,6 +547,8 @@ struct NoAllocDevice {
   uint8_t* scratch;   // device address of g_noalloc_scratch on this device
   int num_sms;
   int gate_up_ctas_per_sm;
+  size_t smem_per_block;
+  bool fused_ok;
 };
 
 std::mutex g_noalloc_mu;
@@ -400,6 +574,12 @@ moe_status_t noalloc_device(int dev, NoAllocDevice* out) {
       return MOE_ERR_CUDA;
     d.scratch = static_cast<uint8_t*>(ptr);
     d.gate_up_ctas_per_sm = std::max(1, occ);
+    moe_decode probe = {};
+    probe.device = dev;
+    probe.num_sms = d.num_sms;
+    probe.cfg.k = 1;
+    if (!query_fused(&probe)) return MOE_ERR_CUDA;
+    d.smem_per_block = probe.smem_per_block;
     d.ready = true;
   }
   *out = d;
@@ -443,6 +623,19 @@ extern "C" moe_status_t moe_decode_layer_noalloc(const moe_decode_config_t* cfg,
   m.gate_up_ctas_per_sm = d.gate_up_ctas_per_sm;
   m.down_smem = (size_t)c.k * c.I * sizeof(float);
   m.d_err = reinterpret_cast<uint32_t*>(d.scratch + kNoAllocHBytes);
+  m.d_bar = reinterpret_cast<unsigned long long*>(d.scratch + kNoAllocHBytes + 8);
+  m.smem_per_block = d.smem_per_block;
+  {
+    // the fused kernel's plan depends on the call's shape
+    moe::FusedParams fp = {};
+    size_t smem = 0;
+    m.fused_ok = true;
+    int occ = 0;
+    m.fused_ok = plan_fused(&m, fp, smem) &&
+                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                     &occ, moe::moe_layer_fused_t1<8>, moe::kFusedThreads, smem) == cudaSuccess &&
+                 occ >= 1 && encode_fused_maps(&m, fp.KC);
+  }
   return moe_decode_layer(&m, T, x, topk_ids, topk_w, reinterpret_cast<uint16_t*>(d.scratch), y,
                           stream);
 }

@@ -42,6 +42,86 @@ __device__ __forceinline__ uint32_t ld_scale(const uint8_t* p) {
 }
 
 // ---------------------------------------------------------------------------
+// TMA bulk copies, mbarriers, named barriers
+// ---------------------------------------------------------------------------
+
+constexpr uint32_t kDeviceTimeout = 0x2u;   // a bounded wait gave up
+constexpr uint32_t kWaitLimit = 1u << 22;   // polls before a spin wait gives up
+// mbarrier waits suspend for up to kWaitSuspendNs per poll (waking as soon as
+// the phase completes) and give up after kMbarPolls polls (about a second)
+constexpr uint32_t kWaitSuspendNs = 20000;
+constexpr uint32_t kMbarPolls = 1u << 16;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// One arrival that also announces `bytes` of copies completing on the barrier.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+
+// Wait for the phase with the given parity to complete. Gives up after
+// kMbarPolls polls, sets kDeviceTimeout in *err and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint32_t* err) {
+  for (uint32_t it = 0; it < kMbarPolls; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(b)), "r"(parity), "r"(kWaitSuspendNs)
+        : "memory");
+    if (done) return true;
+  }
+  atomicOr(err, kDeviceTimeout);
+  return false;
+}
+
+// Global -> shared bulk copy completing on an mbarrier. Source and
+// destination 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 2D tile of a tensor map (x = innermost coordinate in elements, y = row) ->
+// shared memory, completing on an mbarrier. x * element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Barrier over `nthreads` threads (whole warps) of the CTA on named barrier `id`.
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // MXFP8 decode
 // ---------------------------------------------------------------------------
 

@@ -203,3 +203,77 @@ def test_bad_arguments_raise(dev):
     mis = torch.zeros(2 * 256 + 8, dtype=torch.bfloat16, device=dev)[8:].view(2, 256)
     with pytest.raises(MoEError):
         s.layer.gate_up(mis, ids)                                                  # 16-byte offset
+
+
+# ---------------------------------------------------------------------------
+# single-token layer calls (one persistent launch for both projections)
+# ---------------------------------------------------------------------------
+
+def _layer_once(s, ids=None, tw=None, x_bits=None):
+    x = bf16_tensor(s.x_bits if x_bits is None else x_bits, s.dev)
+    di = torch.from_numpy(np.ascontiguousarray(s.ids if ids is None else ids, dtype=np.int32)).to(s.dev)
+    dw = torch.from_numpy(np.ascontiguousarray(s.tw if tw is None else tw, dtype=np.float32)).to(s.dev)
+    h = torch.full((1, s.w.k, s.w.I), float("nan"), dtype=torch.bfloat16, device=s.dev)
+    y = s.layer.layer(x, di, dw, h=h)
+    torch.cuda.synchronize()
+    return h, y
+
+
+@pytest.mark.parametrize("E,k,H,I", [(8, 2, 512, 128), (16, 4, 1024, 256), (64, 8, 2048, 768),
+                                     (12, 8, 7168, 2048), (6, 5, 1536, 384)])
+def test_single_token_layer_matches_oracle(dev, E, k, H, I):
+    s = Small(dev, E, k, H, I, 1, seed=E + H)
+    h, y = _layer_once(s)
+    r = s.ref()
+    assert_within(tensor_to_f64(h), r["h_spec"], tol_h(r["h_spec"]), "h")
+    assert_within(tensor_to_f64(y), r["y_spec"], tol_y(r["y_spec"]), "y")
+    # the two-kernel path on the same inputs agrees within the same bound
+    _, y2 = s.run()
+    assert_within(tensor_to_f64(y2), r["y_spec"], tol_y(r["y_spec"]), "y two-kernel")
+    assert s.layer.get_error() == 0
+
+
+def test_single_token_layer_duplicates_and_bad_ids(dev):
+    from sparse_expert_gemv_gb300 import MOE_DEVICE_BAD_ID
+    s = Small(dev, 16, 4, 1024, 256, 1, seed=3)
+    ids = s.ids.copy()
+    ids[0, 1] = ids[0, 0]          # duplicate
+    ids[0, 3] = 99                 # out of range
+    h, y = _layer_once(s, ids=ids)
+    r = s.ref(ids=ids)
+    assert np.all(tensor_to_f64(h)[0, 3] == 0)
+    assert_within(tensor_to_f64(h), r["h_spec"], tol_h(r["h_spec"]), "h")
+    assert_within(tensor_to_f64(y), r["y_spec"], tol_y(r["y_spec"]), "y")
+    assert s.layer.get_error() == MOE_DEVICE_BAD_ID
+    # every id out of range: y is all zeros
+    h, y = _layer_once(s, ids=np.full((1, 4), -1, np.int32))
+    assert torch.count_nonzero(y).item() == 0
+    assert torch.count_nonzero(h).item() == 0
+    assert s.layer.get_error() == MOE_DEVICE_BAD_ID
+    # and the next call is fine again
+    h, y = _layer_once(s)
+    r = s.ref()
+    assert_within(tensor_to_f64(y), r["y_spec"], tol_y(r["y_spec"]), "y after")
+    assert s.layer.get_error() == 0
+
+
+def test_single_token_layer_graph_replays(dev):
+    s = Small(dev, 64, 8, 2048, 768, 1, seed=11)
+    x = bf16_tensor(s.x_bits, dev)
+    ids = torch.from_numpy(s.ids).to(dev)
+    tw = torch.from_numpy(s.tw).to(dev)
+    h = torch.empty((1, 8, 768), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((1, 2048), dtype=torch.bfloat16, device=dev)
+    s.layer.layer(x, ids, tw, h=h, y=y)
+    torch.cuda.synchronize()
+    ref = y.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(3):
+            s.layer.layer(x, ids, tw, h=h, y=y)
+    for _ in range(4):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+    assert s.layer.get_error() == 0
