@@ -34,9 +34,10 @@
  *     moe_decode_get_error. Nothing traps and nothing spins.
  *   - Duplicate ids in a token's row are legal; their contributions add.
  *   - Results are bitwise reproducible run to run (no atomics on data).
- *   - Calls on one handle may run concurrently on different streams: the
- *     handle holds no per-call device state except the error word (and the
- *     staging buffers of moe_decode_forward_host, which serialises itself).
+ *   - Calls on one handle may run concurrently on different streams, with two
+ *     exceptions: moe_decode_layer with T = 1 (its one-launch form shares the
+ *     handle's grid-barrier counter, so such calls must be ordered on one
+ *     stream) and moe_decode_forward_host (which shares staging buffers).
  */
 #ifndef MOE_DECODE_H
 #define MOE_DECODE_H
@@ -58,6 +59,7 @@ typedef enum {
 
 /* Bits of the device error word. */
 #define MOE_DEVICE_BAD_ID 0x1u     /* some topk_id was outside [0, E) */
+#define MOE_DEVICE_TIMEOUT 0x2u    /* a bounded device wait gave up (results undefined) */
 
 /* Flags of moe_decode_config_t. */
 #define MOE_FLAG_NO_PDL 0x1u       /* launch without programmatic dependent launch */
@@ -81,9 +83,11 @@ typedef struct moe_decode* moe_decode_t;
  *   w_down    device uint8 [E, H, I]    E4M3 codes
  *   s_down    device uint8 [E, H, I/32] UE8M0 scale codes
  * w_gateup and w_down must be 32-byte aligned (rows are then 32-byte aligned
- * too); the scale arrays need no alignment. Allocates a 4-byte device error
- * word (and, when max_T > 0, the staging buffers of
- * moe_decode_forward_host). *out receives the handle; on error *out is NULL.
+ * too); the scale arrays need no alignment (16-byte aligned scale arrays
+ * enable the one-launch single-token layer). Allocates 16 bytes of device
+ * state (the error word and a grid-barrier counter) and, when max_T > 0, the
+ * staging buffers of moe_decode_forward_host. *out receives the handle; on
+ * error *out is NULL.
  */
 moe_status_t moe_decode_create(const moe_decode_config_t* cfg,
                                const uint8_t* w_gateup, const uint8_t* s_gateup,
@@ -153,6 +157,12 @@ moe_status_t moe_down(moe_decode_t handle, int32_t T, const uint16_t* h,
  * drains; topk_ids and topk_w must therefore be complete before this call's
  * work starts on `stream`, which stream order guarantees. h is the caller's
  * [T, k, I] bf16 buffer (32-byte aligned).
+ * With T = 1, when moe_decode_fused_layer(handle) is 1, both projections run
+ * as one cooperative launch of one CTA per SM (kernel moe_layer_fused_t1): a
+ * producer warp streams the CTA's gate/up and then down weight rows with TMA,
+ * and the CTAs meet at a grid barrier (a bounded wait; on timeout it sets
+ * MOE_DEVICE_TIMEOUT) once h is written. Such calls on one handle must not
+ * run concurrently.
  */
 moe_status_t moe_decode_layer(moe_decode_t handle, int32_t T, const uint16_t* x,
                               const int32_t* topk_ids, const float* topk_w,
@@ -182,6 +192,16 @@ const char* moe_status_string(moe_status_t status);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t moe_decode_version(void);
+
+/*
+ * Diagnostic: 1 when moe_decode_layer with T = 1 runs as one persistent
+ * launch (both projections in one cooperative kernel, TMA-streamed weights,
+ * a grid barrier between them) for this handle, 0 when it falls back to the
+ * two kernels (shape or alignment outside that kernel's limits: H a multiple
+ * of 512, I a multiple of 128, scale arrays 16-byte aligned, enough shared
+ * memory), -1 for a NULL handle.
+ */
+int32_t moe_decode_fused_layer(moe_decode_t handle);
 
 /*
  * The whole layer without any device allocation. The pages have no

@@ -118,7 +118,7 @@ bool plan_fused(const moe_decode* m, moe::FusedParams& fp, size_t& smem) {
   if (!m->fused_ok || c.H % 512 || c.I % 128 || !aligned(m->sgu, 16) || !aligned(m->sd, 16))
     return false;
   const int KC = (c.H % 1024 == 0) ? 1024 : 512;       // one TMA box row is <= 1 KB
-  const size_t slot = round_up((size_t)33 * KC, 128);   // 2 x 16 rows of codes + scales
+  const size_t slot = round_up((size_t)moe::GuStageLayout(KC).end, 128);
   const int nbI = c.I / 32;
   const int RG = 16 / gcd_int(16, nbI);
   if (c.H % RG) return false;
@@ -521,6 +521,8 @@ const char* moe_status_string(moe_status_t status) {
 }
 
 int32_t moe_decode_version(void) { return kVersion; }
+
+int32_t moe_decode_fused_layer(moe_decode_t m) { return m ? (m->fused_ok ? 1 : 0) : -1; }
 
 }  // extern "C"
 

@@ -11,7 +11,7 @@
 // them, of the CTA's down rows for every routed expert, into one ring of
 // shared-memory slots guarded by mbarriers. HBM therefore never waits for the
 // gate/up arithmetic to finish before the down weights are requested: by the
-// time the sixteen consumer warps have written h and passed the grid barrier,
+// time the fifteen consumer warps have written h and passed the grid barrier,
 // their down rows are already in shared memory.
 #pragma once
 
@@ -21,13 +21,15 @@
 
 namespace moe {
 
-constexpr int kFusedConsumers = 16;                       // consumer warps
+// 15 consumer warps + 1 producer warp: 4 warps per SM sub-partition, so each
+// thread may hold up to 128 registers (a sub-partition has 16K).
+constexpr int kFusedConsumers = 15;                       // consumer warps
 constexpr int kFusedThreads = (kFusedConsumers + 1) * 32; // + one producer warp
 constexpr int kFusedNeurons = kFusedConsumers;            // gate/up neurons per stage
 
 struct FusedParams {
   // W_gateup codes and scales as 2D uint32 tensors ([E*2I, H/4] and
-  // [E*2I, H/128]), boxes of 16 rows x KC codes (x KC/32 scale bytes)
+  // [E*2I, H/128]), boxes of kFusedNeurons rows x KC codes (x KC/32 scale bytes)
   CUtensorMap tm_codes;
   CUtensorMap tm_scales;
   const uint16_t* x;          // [1, H] bf16
@@ -49,6 +51,19 @@ struct FusedParams {
   int RC;           // down rows per stage (multiple of RG, <= kFusedConsumers)
   int GE;           // experts per down stage
   int EB;           // bytes per expert inside a down stage (multiple of 16)
+};
+
+// Byte offsets of a gate/up stage in a ring slot: gate codes, up codes, gate
+// scales, up scales, each region starting on a 128-byte boundary (the TMA
+// tensor copies that fill them require it); `end` is the bytes used.
+struct GuStageLayout {
+  int up, gs, us, end;
+  __host__ __device__ static constexpr int r128(int v) { return (v + 127) / 128 * 128; }
+  __host__ __device__ explicit GuStageLayout(int KC)
+      : up(r128(kFusedNeurons * KC)),
+        gs(2 * r128(kFusedNeurons * KC)),
+        us(2 * r128(kFusedNeurons * KC) + r128(kFusedNeurons * (KC >> 5))),
+        end(2 * r128(kFusedNeurons * KC) + 2 * r128(kFusedNeurons * (KC >> 5))) {}
 };
 
 // float4 slot of quarter jj of piece q (16 FP32 values): an XOR swizzle so that
@@ -95,7 +110,7 @@ __device__ __forceinline__ void stage_f32_pieces(const uint16_t* __restrict__ sr
   }
 }
 
-// The CTA's stage sequence: gate/up stages (16 neurons of one expert over a
+// The CTA's stage sequence: gate/up stages (15 neurons of one expert over a
 // K-chunk), then down stages (a chunk of the CTA's rows for up to GE unique
 // experts). Producer and consumers run the same warp-uniform walk.
 struct FusedWalk {
@@ -194,7 +209,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* bar, uint32_t* 
 }
 
 template <int KMAX>
-__global__ void __maxnreg__(120) moe_layer_fused_t1(const __grid_constant__ FusedParams p) {
+__global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = p.H, I = p.I, KC = p.KC, S = p.S, nbI = I >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,7 +218,7 @@ __global__ void __maxnreg__(120) moe_layer_fused_t1(const __grid_constant__ Fuse
   float4* hs = xs + (H >> 2);                                                  // [k*I/4]
   uint64_t* full = reinterpret_cast<uint64_t*>(hs + ((size_t)p.k * I >> 2));
   uint64_t* empty = full + S;
-  uint32_t* sm_words = reinterpret_cast<uint32_t*>(empty + S);                // [17][32]
+  uint32_t* sm_words = reinterpret_cast<uint32_t*>(empty + S);                // [16][32]
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
@@ -217,8 +232,8 @@ __global__ void __maxnreg__(120) moe_layer_fused_t1(const __grid_constant__ Fuse
   WarpSchedule<KMAX> s;
   s.build(p.ids, 1, p.k, p.E, sm_words + warp * 32, p.err);
   // gate/up stage layout: gate codes, up codes, gate scales, up scales
-  const int o_up = kFusedNeurons * KC, o_gs = 2 * kFusedNeurons * KC,
-            o_us = 2 * kFusedNeurons * KC + kFusedNeurons * (KC >> 5);
+  const GuStageLayout lay(KC);
+  const int o_up = lay.up, o_gs = lay.gs, o_us = lay.us;
 
   if (warp == kFusedConsumers) {
     // ------------------------------------------------------------ producer
@@ -234,7 +249,7 @@ __global__ void __maxnreg__(120) moe_layer_fused_t1(const __grid_constant__ Fuse
       if (lane == 0) {
         if (st >= S) ok = mbar_wait(&empty[slot], ((st / S) - 1) & 1, p.err);
         if (ok && !wk.down) {
-          // four tensor copies: 16 gate rows, 16 up rows, and their scales
+          // four tensor copies: the stage's gate rows, up rows, and their scales
           // (full boxes; rows past the expert are never read)
           mbar_expect_tx(&full[slot], 2u * kFusedNeurons * KC + 2u * kFusedNeurons * (KC >> 5));
           const int row = e * 2 * I + wk.i0;
@@ -276,7 +291,7 @@ __global__ void __maxnreg__(120) moe_layer_fused_t1(const __grid_constant__ Fuse
   }
 
   // -------------------------------------------------------------- consumers
-  const int ctid = threadIdx.x;                    // 0 .. 511
+  const int ctid = threadIdx.x;                    // consumer thread index
   const int ncons = kFusedConsumers * 32;
   // this lane's routing weight (lane j < k holds w[j]); out-of-range ids give
   // h = 0 (written by the CTA that owns no neuron: CTA 0) and no down term

@@ -77,6 +77,11 @@ class MoEDecode:
     def handle(self) -> ctypes.c_void_p:
         return self._h
 
+    @property
+    def fused_single_token(self) -> bool:
+        """True when one-token layer calls run as one persistent launch."""
+        return lib.moe_decode_fused_layer(self._h) == 1
+
     def _dev(self, shape, dtype, out, name):
         if out is None:
             return torch.empty(shape, dtype=dtype, device=self._weights[0].device)

@@ -223,6 +223,7 @@ def _layer_once(s, ids=None, tw=None, x_bits=None):
                                      (12, 8, 7168, 2048), (6, 5, 1536, 384)])
 def test_single_token_layer_matches_oracle(dev, E, k, H, I):
     s = Small(dev, E, k, H, I, 1, seed=E + H)
+    assert s.layer.fused_single_token, "one-token layer calls should run as one launch here"
     h, y = _layer_once(s)
     r = s.ref()
     assert_within(tensor_to_f64(h), r["h_spec"], tol_h(r["h_spec"]), "h")
@@ -236,6 +237,7 @@ def test_single_token_layer_matches_oracle(dev, E, k, H, I):
 def test_single_token_layer_duplicates_and_bad_ids(dev):
     from sparse_expert_gemv_gb300 import MOE_DEVICE_BAD_ID
     s = Small(dev, 16, 4, 1024, 256, 1, seed=3)
+    assert s.layer.fused_single_token
     ids = s.ids.copy()
     ids[0, 1] = ids[0, 0]          # duplicate
     ids[0, 3] = 99                 # out of range
@@ -259,6 +261,7 @@ def test_single_token_layer_duplicates_and_bad_ids(dev):
 
 def test_single_token_layer_graph_replays(dev):
     s = Small(dev, 64, 8, 2048, 768, 1, seed=11)
+    assert s.layer.fused_single_token
     x = bf16_tensor(s.x_bits, dev)
     ids = torch.from_numpy(s.ids).to(dev)
     tw = torch.from_numpy(s.tw).to(dev)
