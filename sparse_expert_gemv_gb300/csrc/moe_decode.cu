@@ -108,7 +108,6 @@ cudaError_t launch_down(const moe_decode* m, const moe::DownParams& p, cudaStrea
 
 // ---- single-token fused layer ----------------------------------------------
 
-size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int gcd_int(int a, int b) { return b ? gcd_int(b, a % b) : a; }
 
 // Ring geometry of moe_layer_fused_t1 for this handle's shape; false when the
@@ -118,28 +117,35 @@ bool plan_fused(const moe_decode* m, moe::FusedParams& fp, size_t& smem) {
   if (!m->fused_ok || c.H % 512 || c.I % 128 || !aligned(m->sgu, 16) || !aligned(m->sd, 16))
     return false;
   const int KC = (c.H % 1024 == 0) ? 1024 : 512;       // one TMA box row is <= 1 KB
-  const size_t slot = round_up((size_t)moe::GuStageLayout(KC).end, 128);
+  const int slot_g = moe::GuStageLayout(KC).end;        // a multiple of 128
   const int nbI = c.I / 32;
   const int RG = 16 / gcd_int(16, nbI);
   if (c.H % RG) return false;
   const int rows_cta = (c.H / RG + m->num_sms - 1) / m->num_sms * RG;
-  int RC = std::min(rows_cta, moe::kFusedConsumers / RG * RG);
+  const int RC = std::min(rows_cta, moe::kFusedConsumers / RG * RG);
   if (RC < RG) return false;
-  const size_t EB = round_up((size_t)RC * (c.I + nbI), 16);
-  const int GE = (int)std::min<size_t>(32, slot / EB);
-  if (GE < 1) return false;
-  const size_t fixed = (size_t)c.H * 4 + (size_t)c.k * c.I * 4 + (moe::kFusedConsumers + 1) * 128;
-  int S = 8;
-  while (S > 2 && (size_t)S * (slot + 16) + fixed > m->smem_per_block) --S;
-  smem = (size_t)S * (slot + 16) + fixed;
-  if (smem > m->smem_per_block) return false;
+  const int slot_d = moe::round128(RC * (c.I + nbI));
+  // one down slot per routed expert of a row chunk
+  const int sd_want = c.k;
+  auto bytes = [&](int SG, int SD) {
+    return (size_t)moe::FusedSmem(SG, slot_g, SD, slot_d, c.H, c.I, c.k).total;
+  };
+  // three gate/up slots keep about 95 KB of tiles in flight per SM; the down
+  // group buffer takes what is left (a whole row chunk of every routed expert
+  // when it fits), then any room after that goes back to the gate/up ring
+  int SG = 3, SD = sd_want;
+  while (SD > 1 && bytes(SG, SD) > m->smem_per_block) --SD;
+  while (SG > 2 && bytes(SG, SD) > m->smem_per_block) --SG;
+  if (bytes(SG, SD) > m->smem_per_block) return false;
+  while (SG < 8 && bytes(SG + 1, SD) <= m->smem_per_block) ++SG;
+  smem = bytes(SG, SD);
   fp.KC = KC;
-  fp.S = S;
-  fp.slot_bytes = (int)slot;
+  fp.SG = SG;
+  fp.slot_g = slot_g;
+  fp.SD = SD;
+  fp.slot_d = slot_d;
   fp.RG = RG;
   fp.RC = RC;
-  fp.GE = GE;
-  fp.EB = (int)EB;
   return true;
 }
 

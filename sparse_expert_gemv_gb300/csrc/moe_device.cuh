@@ -93,6 +93,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint32_t
   return false;
 }
 
+// Whether the phase with the given parity has completed, without waiting.
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(b)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Global -> shared bulk copy completing on an mbarrier. Source and
 // destination 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
