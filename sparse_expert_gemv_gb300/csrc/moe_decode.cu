@@ -38,10 +38,13 @@ struct moe_decode {
   size_t down_smem;
   size_t smem_per_block;          // opt-in shared-memory maximum of one CTA
   bool fused_ok;                  // the single-token fused kernel can run here
-  CUtensorMap tm_codes;           // W_gateup codes / scales as 2D tensors for its TMA
-  CUtensorMap tm_scales;
+  CUtensorMap tm_codes;           // W_gateup codes / scales and W_down codes / scales
+  CUtensorMap tm_scales;          // as tensors for its TMA copies
+  CUtensorMap tm_dcodes;
+  CUtensorMap tm_dscales;
   uint32_t* d_err;                // device error word (4 bytes) ...
-  unsigned long long* d_bar;      // ... and, 8 bytes on, the fused kernel's grid barrier
+  unsigned long long* d_bar;      // ... then, 8 and 16 bytes on, the fused kernel's launch
+                                  // and grid-barrier counters
   // staging buffers of moe_decode_forward_host (max_T tokens)
   uint16_t* d_x;
   int32_t* d_ids;
@@ -116,7 +119,8 @@ bool plan_fused(const moe_decode* m, moe::FusedParams& fp, size_t& smem) {
   const moe_decode_config_t& c = m->cfg;
   if (!m->fused_ok || c.H % 512 || c.I % 128 || !aligned(m->sgu, 16) || !aligned(m->sd, 16))
     return false;
-  const int KC = (c.H % 1024 == 0) ? 1024 : 512;       // one TMA box row is <= 1 KB
+  // a stage's K-chunk: whole 2 KB rows when H allows, else 1 KB or 512 B
+  const int KC = (c.H % 2048 == 0) ? 2048 : (c.H % 1024 == 0) ? 1024 : 512;
   const int slot_g = moe::GuStageLayout(KC).end;        // a multiple of 128
   const int nbI = c.I / 32;
   const int RG = 16 / gcd_int(16, nbI);
@@ -125,21 +129,19 @@ bool plan_fused(const moe_decode* m, moe::FusedParams& fp, size_t& smem) {
   const int RC = std::min(rows_cta, moe::kFusedConsumers / RG * RG);
   if (RC < RG) return false;
   const int slot_d = moe::round128(RC * (c.I + nbI));
-  // one down slot per routed expert of a row chunk
-  const int sd_want = c.k;
   auto bytes = [&](int SG, int SD) {
     return (size_t)moe::FusedSmem(SG, slot_g, SD, slot_d, c.H, c.I, c.k).total;
   };
-  // three gate/up slots keep about 95 KB of tiles in flight per SM; the down
-  // group buffer takes what is left (a whole row chunk of every routed expert
-  // when it fits), then any room after that goes back to the gate/up ring
-  int SG = 3, SD = sd_want;
+  // two gate/up slots (up to ~125 KB of tiles in flight per SM), then the
+  // down group buffer as large as fits (every routed expert's row chunk when
+  // it can), then any room left goes back to the gate/up ring
+  int SG = 2, SD = c.k;
   while (SD > 1 && bytes(SG, SD) > m->smem_per_block) --SD;
-  while (SG > 2 && bytes(SG, SD) > m->smem_per_block) --SG;
   if (bytes(SG, SD) > m->smem_per_block) return false;
   while (SG < 8 && bytes(SG + 1, SD) <= m->smem_per_block) ++SG;
   smem = bytes(SG, SD);
   fp.KC = KC;
+  fp.kin = std::min(256, KC / 4);
   fp.SG = SG;
   fp.slot_g = slot_g;
   fp.SD = SD;
@@ -179,14 +181,53 @@ bool encode_u32_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t ro
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The W_gateup tensor maps of the fused kernel (codes [E*2I, H/4] uint32,
-// scales [E*2I, H/128] uint32; boxes of 16 rows by KC codes / KC/32 scales).
-bool encode_fused_maps(moe_decode* m, int KC) {
+// A [rows, n1, n0] uint32 tensor (n0 innermost, rows `pitch` bytes apart),
+// read in boxes of box_rows x b1 x n0.
+bool encode_u32_3d(CUtensorMap* tm, const void* base, uint64_t n0, uint64_t n1, uint64_t rows,
+                   uint64_t pitch, uint32_t b1, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {n0, n1, rows};
+  cuuint64_t strides[2] = {n0 * 4, pitch};
+  cuuint32_t box[3] = {(cuuint32_t)n0, b1, box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A [n3, n2, n1, n0] uint32 tensor (n0 innermost, dense), read in boxes of
+// 1 x b2 x n1 x n0.
+bool encode_u32_4d(CUtensorMap* tm, const void* base, uint64_t n0, uint64_t n1, uint64_t n2,
+                   uint64_t n3, uint32_t b2) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {n0, n1, n2, n3};
+  cuuint64_t strides[3] = {n0 * 4, n0 * n1 * 4, n0 * n1 * n2 * 4};
+  cuuint32_t box[4] = {(cuuint32_t)n0, (cuuint32_t)n1, b2, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The fused kernel's tensor maps. W_gateup codes as [E*2I][H/(4*kin)][kin]
+// uint32 with boxes of kFusedNeurons rows x KC codes, its scales as
+// [E*2I][H/128] uint32 with boxes of kFusedNeurons rows x KC/32 scale bytes;
+// W_down codes as [E][H][I/(4*kin_d)][kin_d] uint32 with boxes of RC rows of
+// one expert, its scales as [E][H*I/128] uint32 with boxes of RC rows.
+bool encode_fused_maps(moe_decode* m, int KC, int RC) {
   const moe_decode_config_t& c = m->cfg;
   const uint64_t rows = (uint64_t)c.E * 2 * c.I;
-  return encode_u32_2d(&m->tm_codes, m->wgu, c.H / 4, rows, c.H, KC / 4, moe::kFusedNeurons) &&
+  const int kin = std::min(256, KC / 4);
+  const int kin_d = std::min(256, c.I / 4);
+  return encode_u32_3d(&m->tm_codes, m->wgu, kin, c.H / (4 * kin), rows, c.H, KC / (4 * kin),
+                       moe::kFusedNeurons) &&
          encode_u32_2d(&m->tm_scales, m->sgu, c.H / 128, rows, c.H / 32, KC / 128,
-                       moe::kFusedNeurons);
+                       moe::kFusedNeurons) &&
+         encode_u32_4d(&m->tm_dcodes, m->wd, kin_d, c.I / (4 * kin_d), c.H, c.E, RC) &&
+         encode_u32_2d(&m->tm_dscales, m->sd, (uint64_t)c.H * c.I / 128, c.E,
+                       (uint64_t)c.H * c.I / 32, RC * c.I / 128, 1);
 }
 
 cudaError_t set_fused_attributes(size_t smem) {
@@ -241,7 +282,7 @@ bool query_fused(moe_decode* m) {
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, moe::moe_layer_fused_t1<8>,
                                                     moe::kFusedThreads, smem) != cudaSuccess)
     return false;
-  m->fused_ok = occ >= 1 && encode_fused_maps(m, fp.KC);
+  m->fused_ok = occ >= 1 && encode_fused_maps(m, fp.KC, fp.RC);
   return true;
 }
 
@@ -261,9 +302,12 @@ moe_status_t fused_layer(moe_decode* m, const uint16_t* x, const int32_t* ids, c
   fp.h = h;
   fp.y = y;
   fp.err = m->d_err;
-  fp.grid_bar = m->d_bar;
+  fp.launch_ctr = m->d_bar;
+  fp.bar_ctr = m->d_bar + 1;
   fp.tm_codes = m->tm_codes;
   fp.tm_scales = m->tm_scales;
+  fp.tm_dcodes = m->tm_dcodes;
+  fp.tm_dscales = m->tm_dscales;
   fp.k = c.k;
   fp.E = c.E;
   fp.H = c.H;
@@ -363,9 +407,11 @@ moe_status_t moe_decode_create(const moe_decode_config_t* cfg, const uint8_t* w_
   bool ok = cudaGetDevice(&m->device) == cudaSuccess &&
             cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) ==
                 cudaSuccess &&
-            cudaMalloc(&m->d_err, 16) == cudaSuccess && cudaMemset(m->d_err, 0, 16) == cudaSuccess;
+            cudaMalloc(&m->d_err, 32) == cudaSuccess && cudaMemset(m->d_err, 0, 32) == cudaSuccess;
   if (ok) m->d_bar = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(m->d_err) + 8);
   ok = ok && query_fused(m);
+
+
   // a per-function limit shared by every handle: always the library's maximum
   ok = ok && cudaFuncSetAttribute(moe::moe_down_3d_batched<kDownQ>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -505,10 +551,7 @@ moe_status_t moe_decode_get_error(moe_decode_t m, uint32_t* device_flags) {
   uint32_t v = 0;
   if (cudaDeviceSynchronize() != cudaSuccess ||
       cudaMemcpy(&v, m->d_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemset(m->d_err, 0, sizeof(v)) != cudaSuccess ||
-      // a wait that gave up may have left the grid barrier's count off a
-      // multiple of the grid size: start it again from zero
-      ((v & moe::kDeviceTimeout) && cudaMemset(m->d_bar, 0, 8) != cudaSuccess))
+      cudaMemset(m->d_err, 0, sizeof(v)) != cudaSuccess)
     return MOE_ERR_CUDA;
   *device_flags = v;
   return v ? MOE_ERR_DEVICE_FAULT : MOE_OK;
@@ -547,7 +590,8 @@ namespace {
 constexpr size_t kNoAllocHBytes = MOE_NOALLOC_SCRATCH_BYTES;
 constexpr int kNoAllocMaxDevices = 64;
 
-// [0, kNoAllocHBytes): h of the current call; then the 4-byte error word.
+// [0, kNoAllocHBytes): h of the current call; then the 4-byte error word and,
+// 8 and 16 bytes on, the fused kernel's launch and grid-barrier counters.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocHBytes + 256];
 
 struct NoAllocDevice {
@@ -642,7 +686,7 @@ extern "C" moe_status_t moe_decode_layer_noalloc(const moe_decode_config_t* cfg,
     m.fused_ok = plan_fused(&m, fp, smem) &&
                  cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                      &occ, moe::moe_layer_fused_t1<8>, moe::kFusedThreads, smem) == cudaSuccess &&
-                 occ >= 1 && encode_fused_maps(&m, fp.KC);
+                 occ >= 1 && encode_fused_maps(&m, fp.KC, fp.RC);
   }
   return moe_decode_layer(&m, T, x, topk_ids, topk_w, reinterpret_cast<uint16_t*>(d.scratch), y,
                           stream);

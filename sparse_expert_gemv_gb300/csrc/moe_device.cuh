@@ -128,6 +128,28 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
       : "memory");
 }
 
+// 3D tile of a tensor map (x innermost, in elements) -> shared memory,
+// completing on an mbarrier. x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 4D tile of a tensor map (x innermost, in elements) -> shared memory,
+// completing on an mbarrier. x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int x, int y, int z, int w,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // Barrier over `nthreads` threads (whole warps) of the CTA on named barrier `id`.
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -264,6 +286,21 @@ struct WarpSchedule {
     const int n = u - __shfl_sync(kFull, excl, L);     // n-th set bit of w (0-based)
     const bool mine = ((w >> lane) & 1u) && (__popc(w & ((1u << lane) - 1u)) == n);
     return L * 32 + (__ffs(__ballot_sync(kFull, mine)) - 1);
+  }
+
+  // Expert id of the u-th unique expert where u differs per lane (every lane
+  // takes part; a lane with u >= n_unique gets an unspecified value): the
+  // owner word is the first whose inclusive prefix count exceeds u, found by
+  // a five-step binary search over the lanes' prefix counts.
+  __device__ __forceinline__ int expert_per_lane(int u) const {
+    const int incl = excl + __popc(word);
+    int L = 0;
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1)
+      if (__shfl_sync(kFull, incl, L + step - 1) <= u) L += step;
+    const uint32_t w = __shfl_sync(kFull, word, L & 31);
+    const int n = u - __shfl_sync(kFull, excl, L & 31);
+    return (L & 31) * 32 + (int)__fns(w, 0, n + 1);
   }
 
   // Bits j of this lane's token whose id equals e.

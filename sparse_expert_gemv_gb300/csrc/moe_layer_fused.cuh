@@ -7,13 +7,22 @@
 // up dot products itself; in the down phase a warp owns one output row.
 //
 // What the single launch adds is the memory stream. One producer warp per CTA
-// feeds two rings of shared-memory slots guarded by mbarriers: the gate/up
-// ring (TMA tensor tiles of fifteen neurons' gate and up rows over a K-chunk)
-// and the down ring (bulk copies of the CTA's output rows of one routed
-// expert). Gate/up tiles go first; whenever the gate/up ring is full the
-// producer fills free down slots instead, so HBM keeps streaming while the
-// consumers compute, and by the time the fifteen consumer warps have written
-// h and passed the grid barrier most of their down rows are already on chip.
+// streams, with TMA, first the CTA's gate/up rows (tiles of fifteen neurons'
+// gate and up rows over a K-chunk, into a ring of SG shared-memory slots
+// guarded by mbarriers), then, right after the last gate/up tile, its down
+// rows for every routed expert into a buffer of their own, so HBM keeps
+// streaming while the consumers compute and the down rows land while h is
+// being exchanged. h itself is staged in the slot of the last gate/up stage
+// (or in its own region when it does not fit there).
+//
+// Every CTA needs every h value, so the CTAs meet at a grid barrier between
+// the phases (the launch is cooperative, so all of them are resident). Each
+// CTA learns the launch's index from one counter add at its start; at the
+// barrier it then only posts a release add to a second counter and polls it
+// (acquire loads) for the value that index implies, one round trip less than
+// a barrier that must read back its own arrival. (Publishing h as
+// epoch-tagged words that readers poll directly measured slower on this
+// part: every CTA polling all of h floods L2 while the down rows stream.)
 //
 // Arithmetic. Each lane reduces one 32-element MX block at a time: 32 E4M3
 // codes against 32 activations, FP32 accumulation, then the block's UE8M0
@@ -40,10 +49,16 @@ constexpr int kFusedThreads = (kFusedConsumers + 1) * 32; // + one producer warp
 constexpr int kFusedNeurons = kFusedConsumers;            // gate/up neurons per stage
 
 struct FusedParams {
-  // W_gateup codes and scales as 2D uint32 tensors ([E*2I, H/4] and
-  // [E*2I, H/128]), boxes of kFusedNeurons rows x KC codes (x KC/32 scale bytes)
+  // W_gateup codes as a 3D uint32 tensor [E*2I][H/(4*kin)][kin] with boxes of
+  // kFusedNeurons rows x KC codes, and its scales as a 2D uint32 tensor
+  // [E*2I][H/128] with boxes of kFusedNeurons rows x KC/32 scale bytes
   CUtensorMap tm_codes;
   CUtensorMap tm_scales;
+  // W_down codes as a 4D uint32 tensor [E][H][I/(4*kin_d)][kin_d] with boxes of
+  // RC rows of one expert, and its scales as a 2D uint32 tensor [E][H*I/128]
+  // with boxes of RC rows' scale bytes (rows past H read as zeros)
+  CUtensorMap tm_dcodes;
+  CUtensorMap tm_dscales;
   const uint16_t* x;          // [1, H] bf16
   const int32_t* ids;         // [1, k]
   const float* w;             // [1, k]
@@ -54,13 +69,15 @@ struct FusedParams {
   uint16_t* h;                // [1, k, I] bf16 (written, then read back through L2)
   uint16_t* y;                // [1, H] bf16
   uint32_t* err;
-  unsigned long long* grid_bar;   // arrivals, grows by gridDim.x per launch
+  unsigned long long* launch_ctr;  // grows by gridDim.x per launch, at kernel start
+  unsigned long long* bar_ctr;     // grows by gridDim.x per launch, at the grid barrier
   int k, E, H, I;
-  int KC;       // gate/up codes per row per stage: 512 or 1024, divides H
+  int KC;       // gate/up codes per row per stage: 512, 1024 or 2048, divides H
+  int kin;      // uint32 words per innermost box row of tm_codes (KC/4 or 256)
   int SG;       // gate/up ring slots
   int slot_g;   // bytes per gate/up slot (GuStageLayout(KC).end)
-  int SD;       // down slots (one routed expert's row chunk each), filled as one group
-  int slot_d;   // bytes per down slot: RC rows of codes, then RC rows of scales
+  int SD;       // routed experts per down group (one row chunk each)
+  int slot_d;   // bytes per expert in a down group: RC rows of codes, then RC rows of scales
   int RG;       // down row granule (keeps scale copies 16-byte aligned)
   int RC;       // down rows per chunk (multiple of RG, <= kFusedConsumers)
 };
@@ -79,38 +96,50 @@ struct GuStageLayout {
         end(2 * round128(kFusedNeurons * KC) + 2 * round128(kFusedNeurons * (KC >> 5))) {}
 };
 
-// Shared-memory map of the kernel (byte offsets, each 128-byte aligned).
+// Shared-memory map of the kernel (byte offsets, each 128-byte aligned). The
+// SG ring slots start at 0; the staged h reuses one of them when it fits.
 struct FusedSmem {
-  int ring_d;   // SD down slots (the SG gate/up slots start at 0)
+  int dg;       // the down group buffer: SD experts x slot_d bytes
   int xs;       // x as f16, [H/32] blocks of 64 bytes (swizzled 16-byte chunks)
   int xf;       // [H/32] FP32 block factors 2^-e of x
-  int hs;       // h of each unique expert as f16, [k][I/32] blocks of 64 bytes
-  int hf;       // [k][I/32] FP32 block factors of h
+  int ep;       // the value bar_ctr reaches when this launch's CTAs have all arrived
   int cf;       // [k] combined routing weight of each unique expert
   int jz;       // [k] first slot j routed to each unique expert
+  int db;       // [32] byte offset of each expert of a down group
   int bars;     // mbarriers: full_g[SG], empty_g[SG], full_d, empty_d
   int words;    // 16 warps x 32 words of expert bitmap
+  // h of each unique expert as f16 ([k][I/32] blocks of 64 bytes), then its
+  // FP32 block factors: at hs_off inside a ring slot when h_bytes <= slot_g,
+  // else at hs_own (a region of its own)
+  int hf_off, h_bytes, hs_own;
   int total;
   __host__ __device__ FusedSmem(int SG, int slot_g, int SD, int slot_d, int H, int I, int k) {
     int o = SG * slot_g;
-    ring_d = o;
+    dg = o;
     o += SD * slot_d;
     xs = o;
     o += round128(H * 2);
     xf = o;
     o += round128((H >> 5) * 4);
-    hs = o;
-    o += round128(k * I * 2);
-    hf = o;
-    o += round128(k * (I >> 5) * 4);
+    ep = o;
+    o += 128;
     cf = o;
     o += round128(k * 4);
     jz = o;
     o += round128(k * 4);
+    db = o;
+    o += 128;
     bars = o;
     o += round128((2 * SG + 2) * 8);
     words = o;
     o += 16 * 32 * 4;
+    hf_off = round128(k * I * 2);
+    h_bytes = hf_off + round128(k * (I >> 5) * 4);
+    hs_own = -1;
+    if (h_bytes > slot_g) {
+      hs_own = o;
+      o += h_bytes;
+    }
     total = o;
   }
 };
@@ -301,16 +330,12 @@ struct RingPos {
   }
 };
 
-// Grid-wide barrier for a cooperative launch: every CTA adds one arrival to a
-// 64-bit counter that grows by gridDim.x per launch (a release at GPU scope,
-// after the CTA's threads met at a named barrier), then polls it with acquire
-// loads (bounded) until this launch's arrivals are complete. Called by one
-// thread per CTA.
-__device__ __forceinline__ bool grid_barrier(unsigned long long* bar, uint32_t* err) {
-  unsigned long long ticket;
-  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(ticket) : "l"(bar) : "memory");
-  const unsigned long long G = gridDim.x;
-  const unsigned long long target = (ticket / G + 1) * G;
+// Grid barrier of a cooperative launch, called by one thread per CTA after the
+// CTA's threads have met: a release add of one arrival (cumulative over what
+// those threads wrote), then bounded acquire polls until all arrived.
+__device__ __forceinline__ bool grid_barrier(unsigned long long* bar, unsigned long long target,
+                                             uint32_t* err) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
   for (uint32_t it = 0; it < kWaitLimit; ++it) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(bar) : "memory");
@@ -327,11 +352,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const FusedSmem L(SG, p.slot_g, p.SD, p.slot_d, H, I, p.k);
   uint8_t* ring_g = smem;
-  uint8_t* ring_d = smem + L.ring_d;
   uint8_t* xs = smem + L.xs;
   float* xf = reinterpret_cast<float*>(smem + L.xf);
-  uint8_t* hs = smem + L.hs;
-  float* hf = reinterpret_cast<float*>(smem + L.hf);
+  int* db = reinterpret_cast<int*>(smem + L.db);
+  unsigned long long* bar_target = reinterpret_cast<unsigned long long*>(smem + L.ep);
   float* cf = reinterpret_cast<float*>(smem + L.cf);
   int* jz = reinterpret_cast<int*>(smem + L.jz);
   uint64_t* full_g = reinterpret_cast<uint64_t*>(smem + L.bars);
@@ -341,6 +365,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   uint32_t* sm_words = reinterpret_cast<uint32_t*>(smem + L.words);
   const int ctid = threadIdx.x;                    // consumer thread index
   const int ncons = kFusedConsumers * 32;
+  if (warp == kFusedConsumers && lane == 0) {
+    // the tensor maps are kernel parameters: fetch them while upstream work drains
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_codes) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_scales) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_dcodes) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_dscales) : "memory");
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < SG; ++i) {
       mbar_init(&full_g[i], 1);
@@ -353,6 +384,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   __syncthreads();
   pdl_wait();      // x, topk_ids and topk_w come from upstream work
   pdl_trigger();
+  if (warp == kFusedConsumers - 1 && lane == 0) {
+    // this launch's index: launches are stream-ordered (and programmatic
+    // dependents wait above for the previous one), so each adds gridDim.x
+    const unsigned long long ticket = atomicAdd(p.launch_ctr, 1ull);
+    *bar_target = (ticket / gridDim.x + 1ull) * gridDim.x;
+  }
+  // slot j's routing weight in lane j of warp 0, loaded before the stream starts
+  const float wj = (warp == 0 && lane < p.k) ? __ldg(p.w + lane) : 0.f;
   if (warp < kFusedConsumers) {
     // x -> f16 blocks first: these loads go out before the weight stream
     for (int b = ctid; b < (H >> 5); b += ncons) {
@@ -370,67 +409,51 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     // ------------------------------------------------------------ producer
     GuWalk gw;
     gw.begin(nU, p);
-    DownWalk dw;
-    dw.begin(nU, p);
     RingPos rg(SG);
-    uint32_t dphase = 0;
-    int gi = 0, dgroups = 0;
+    int gi = 0;
     bool ok = true;
-    while (gw.valid || dw.valid) {
-      // 1: a gate/up stage, 2: a down group
-      int what = 0;
-      if (gw.valid) {
-        bool free_slot = gi < SG;
-        if (!free_slot && lane == 0) free_slot = mbar_test(&empty_g[rg.slot], rg.phase ^ 1u);
-        if (__shfl_sync(kFull, free_slot, 0)) what = 1;
-      }
-      // the first down group's buffer is free from the start; later groups are
-      // only waited for once no gate/up stage is left (their consumers come after)
-      if (!what && dw.valid && (dgroups == 0 || !gw.valid)) what = 2;
-      if (!what) {
-        if (lane == 0) ok = mbar_wait(&empty_g[rg.slot], rg.phase ^ 1u, p.err);
-        ok = __shfl_sync(kFull, ok, 0);
-        if (!ok) break;
-        what = 1;
-      }
-      if (what == 1) {
-        const int e = s.expert(gw.u);   // warp-collective
-        if (lane == 0) {
-          uint8_t* dst = ring_g + (size_t)rg.slot * p.slot_g;
-          uint64_t* bar = &full_g[rg.slot];
-          // four tensor copies: the stage's gate rows, up rows, and their scales
-          // (full boxes; rows past the expert are never read)
-          mbar_expect_tx(bar, 2u * kFusedNeurons * KC + 2u * kFusedNeurons * (KC >> 5));
-          const int row = e * 2 * I + gw.i0;
-          tma_load_2d(dst, &p.tm_codes, gw.kc * (KC >> 2), row, bar);
-          tma_load_2d(dst + lay.up, &p.tm_codes, gw.kc * (KC >> 2), row + I, bar);
-          tma_load_2d(dst + lay.gs, &p.tm_scales, gw.kc * (KC >> 7), row, bar);
-          tma_load_2d(dst + lay.us, &p.tm_scales, gw.kc * (KC >> 7), row + I, bar);
-        }
-        gw.next();
-        rg.next();
-        ++gi;
-      } else {
-        if (lane == 0 && dgroups > 0) ok = mbar_wait(empty_d, dphase ^ 1u, p.err);
-        ok = __shfl_sync(kFull, ok, 0);
-        if (!ok) break;
-        const uint32_t cb = (uint32_t)dw.rc * I, sb = (uint32_t)dw.rc * nbI;
-        if (lane == 0) mbar_expect_tx(full_d, (cb + sb) * dw.ng);
-        for (int gi2 = 0; gi2 < dw.ng; ++gi2) {
-          const int e = s.expert(dw.u0 + gi2);   // warp-collective
-          if (lane == 0) {
-            uint8_t* dst = ring_d + (size_t)gi2 * p.slot_d;
-            const size_t row = (size_t)e * H + dw.c0;
-            bulk_copy_g2s(dst, p.wd + row * I, cb, full_d);
-            bulk_copy_g2s(dst + (size_t)p.RC * I, p.sd + row * nbI, sb, full_d);
-          }
-        }
-        dw.next();
-        dphase ^= 1u;
-        ++dgroups;
+    for (; gw.valid; gw.next(), rg.next(), ++gi) {
+      if (lane == 0 && gi >= SG) ok = mbar_wait(&empty_g[rg.slot], rg.phase ^ 1u, p.err);
+      ok = __shfl_sync(kFull, ok, 0);
+      if (!ok) break;
+      const int e = s.expert(gw.u);   // warp-collective
+      if (lane == 0) {
+        uint8_t* dst = ring_g + (size_t)rg.slot * p.slot_g;
+        uint64_t* bar = &full_g[rg.slot];
+        // four tensor copies: the stage's gate rows, up rows, and their scales
+        // (full boxes; rows past the expert are never read)
+        mbar_expect_tx(bar, 2u * kFusedNeurons * KC + 2u * kFusedNeurons * (KC >> 5));
+        const int row = e * 2 * I + gw.i0;
+        const int kchunk = gw.kc * ((KC >> 2) / p.kin);
+        tma_load_3d(dst, &p.tm_codes, 0, kchunk, row, bar);
+        tma_load_3d(dst + lay.up, &p.tm_codes, 0, kchunk, row + I, bar);
+        tma_load_2d(dst + lay.gs, &p.tm_scales, gw.kc * (KC >> 7), row, bar);
+        tma_load_2d(dst + lay.us, &p.tm_scales, gw.kc * (KC >> 7), row + I, bar);
       }
     }
-    // never leave with copies in flight: the last stages of each ring must land
+    // down groups, right behind the last gate/up tile (the first group's
+    // buffer is free; each later one waits for the previous to be consumed)
+    DownWalk dw;
+    dw.begin(nU, p);
+    uint32_t dphase = 0;
+    int dgroups = 0;
+    for (; ok && dw.valid; dw.next(), dphase ^= 1u, ++dgroups) {
+      if (lane == 0 && dgroups > 0) ok = mbar_wait(empty_d, dphase ^ 1u, p.err);
+      ok = __shfl_sync(kFull, ok, 0);
+      if (!ok) break;
+      // two tensor copies per expert: RC rows of codes and their scales (full
+      // boxes: rows of the next chunk, or zeros past H, are never read)
+      if (lane == 0) mbar_expect_tx(full_d, (uint32_t)p.RC * (I + nbI) * dw.ng);
+      for (int ui = 0; ui < dw.ng; ++ui) {
+        const int e = s.expert(dw.u0 + ui);   // warp-collective
+        if (lane == 0) {
+          uint8_t* dst = smem + L.dg + (size_t)ui * p.slot_d;
+          tma_load_4d(dst, &p.tm_dcodes, 0, 0, dw.c0, e, full_d);
+          tma_load_2d(dst + (size_t)p.RC * I, &p.tm_dscales, dw.c0 * (nbI >> 2), e, full_d);
+        }
+      }
+    }
+    // never leave with copies in flight
     if (lane == 0) {
       RingPos r(SG);
       for (int d = 0; d < gi; ++d, r.next())
@@ -442,27 +465,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
 
   // -------------------------------------------------------------- consumers
   named_sync(1, ncons);   // x staged
-  // per unique expert: the combined routing weight of its slots and the first
-  // slot routed to it (its h row); out-of-range ids give h = 0 (written by
-  // CTA 0) and no down term
-  if (warp == 0) {
-    const float wj = (lane < p.k) ? __ldg(p.w + lane) : 0.f;
-    for (int u = 0; u < nU; ++u) {
-      const int e = s.expert(u);
-      const uint32_t jm = __shfl_sync(kFull, s.jmask(e), 0);   // lane 0 holds the token
-      const float c = warp_sum(((jm >> lane) & 1u) ? wj : 0.f);
-      if (lane == 0) {
-        cf[u] = c;
-        jz[u] = __ffs(jm) - 1;
-      }
-    }
-    if (blockIdx.x == 0 && s.badmask) {
-      for (uint32_t m = s.badmask; m; m &= m - 1) {
-        uint16_t* row = p.h + (size_t)(__ffs(m) - 1) * I;
-        for (int i = 0; i < I; ++i) row[i] = 0;   // lane 0 alone holds the token
-      }
-    }
-  }
 
   const LaneBlock lb(lane);
   // a warp whose bounded wait gave up stops waiting and computing but still
@@ -470,10 +472,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   bool dead = false;
 
   // ---- gate/up: warp owns neuron i0 + warp of each stage, lane owns block lane
+  RingPos rg(SG);
   {
     GuWalk gw;
     gw.begin(nU, p);
-    RingPos rg(SG);
     float ag = 0.f, au = 0.f;
     const int nbk = KC >> 5;                      // blocks per row per stage
     for (; gw.valid; gw.next(), rg.next()) {
@@ -506,9 +508,43 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     }
   }
 
-  // every h value of every CTA is written before any CTA reads h
+  if (warp == 0) {
+    // per unique expert u (lane u): the combined routing weight of its slots
+    // and the first slot routed to it (its h row); out-of-range ids give h = 0
+    // (written by CTA 0) and no down term
+    const int e = s.expert_per_lane(lane);
+    uint32_t jm = 0;
+    float c = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      const int idj = __shfl_sync(kFull, s.id[j], 0);    // lane 0 holds the token
+      const float wjj = __shfl_sync(kFull, wj, j);
+      if (j < p.k && idj == e) {
+        jm |= 1u << j;
+        c += wjj;
+      }
+    }
+    if (lane < nU) {
+      cf[lane] = c;
+      jz[lane] = __ffs(jm) - 1;
+    }
+    if (blockIdx.x == 0) {
+      const uint32_t bad = __shfl_sync(kFull, s.badmask, 0);
+      for (uint32_t m = bad; m; m &= m - 1) {
+        uint16_t* row = p.h + (size_t)(__ffs(m) - 1) * I;
+        for (int i = lane; i < I; i += 32) row[i] = 0;
+      }
+    }
+  }
+  // the slot of the last gate/up stage holds the staged h
+  const int s_last = (rg.slot + SG - 1) % SG;
+  uint8_t* hs = L.hs_own >= 0 ? smem + L.hs_own : ring_g + (size_t)s_last * p.slot_g;
+  float* hf = reinterpret_cast<float*>(hs + L.hf_off);
+  if (ctid < 32) db[ctid] = L.dg + ctid * p.slot_d;
+  // every h value of every CTA is written before any CTA reads h (and the
+  // last gate/up stage's slot is idle once every consumer is past it)
   named_sync(1, ncons);
-  if (ctid == 0 && !grid_barrier(p.grid_bar, p.err)) dead = true;
+  if (ctid == 0 && !grid_barrier(p.bar_ctr, *bar_target, p.err)) dead = true;
   named_sync(1, ncons);
   // h of each unique expert -> f16 blocks (read through L2: other CTAs wrote it)
   for (int t = ctid; t < nU * nbI; t += ncons) {
@@ -538,10 +574,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
           int ui2 = ui, b2 = b + 32;
           while (b2 >= nbI) { b2 -= nbI; ++ui2; }
           const bool two = t + 32 < n_items;
-          const uint8_t* s1 = ring_d + (size_t)ui * p.slot_d;
+          const uint8_t* s1 = smem + db[ui];
           const float d1 = dot_block(s1 + (size_t)warp * I + 32 * b, hs + (size_t)(dw.u0 + ui) * nbI * 64 + 64 * b, lb);
           float d2 = 0.f;
-          const uint8_t* s2 = ring_d + (size_t)ui2 * p.slot_d;
+          const uint8_t* s2 = smem + db[ui2 < 32 ? ui2 : 0];
           if (two) d2 = dot_block(s2 + (size_t)warp * I + 32 * b2, hs + (size_t)(dw.u0 + ui2) * nbI * 64 + 64 * b2, lb);
           const float v1 = d1 * hf[(dw.u0 + ui) * nbI + b] * ue8m0_to_f32(s1[(size_t)p.RC * I + warp * nbI + b]);
           acc = fmaf(v1, cf[dw.u0 + ui], acc);
