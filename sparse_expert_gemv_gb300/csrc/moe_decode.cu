@@ -231,11 +231,11 @@ bool encode_fused_maps(moe_decode* m, int KC, int RC) {
 }
 
 cudaError_t set_fused_attributes(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(moe::moe_layer_fused_t1<8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(moe::moe_layer_fused_t1<32>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaSuccess;
+  for (const void* f : {(const void*)moe::moe_layer_fused_t1<8>,
+                        (const void*)moe::moe_layer_fused_t1<32>})
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   return e;
 }
 

@@ -79,6 +79,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
 // Wait for the phase with the given parity to complete. Gives up after
 // kMbarPolls polls, sets kDeviceTimeout in *err and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint32_t* err) {
+#pragma unroll 1
   for (uint32_t it = 0; it < kMbarPolls; ++it) {
     uint32_t done;
     asm volatile(

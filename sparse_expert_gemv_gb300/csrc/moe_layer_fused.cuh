@@ -262,7 +262,8 @@ struct GuWalk {
   __device__ __forceinline__ void begin(int nU, const FusedParams& p) {
     I = p.I;
     nkc = p.H / p.KC;
-    const long long G = (long long)nU * I;
+    // 32-bit: nU * I * gridDim.x stays far below 2^32 for every supported shape
+    const uint32_t G = (uint32_t)nU * (uint32_t)I;
     g = (int)(G * blockIdx.x / gridDim.x);
     g1 = (int)(G * (blockIdx.x + 1) / gridDim.x);
     u = g / I;
@@ -292,9 +293,9 @@ struct DownWalk {
   bool valid;
 
   __device__ __forceinline__ void begin(int nU_, const FusedParams& p) {
-    const int nrg = p.H / p.RG;
-    r0 = (int)((long long)nrg * blockIdx.x / gridDim.x) * p.RG;
-    r1 = (int)((long long)nrg * (blockIdx.x + 1) / gridDim.x) * p.RG;
+    const uint32_t nrg = (uint32_t)(p.H / p.RG);
+    r0 = (int)(nrg * blockIdx.x / gridDim.x) * p.RG;
+    r1 = (int)(nrg * (blockIdx.x + 1) / gridDim.x) * p.RG;
     nU = nU_;
     RC = p.RC;
     SD = p.SD;
@@ -336,6 +337,7 @@ struct RingPos {
 __device__ __forceinline__ bool grid_barrier(unsigned long long* bar, unsigned long long target,
                                              uint32_t* err) {
   asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
+#pragma unroll 1
   for (uint32_t it = 0; it < kWaitLimit; ++it) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(bar) : "memory");
@@ -394,6 +396,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   const float wj = (warp == 0 && lane < p.k) ? __ldg(p.w + lane) : 0.f;
   if (warp < kFusedConsumers) {
     // x -> f16 blocks first: these loads go out before the weight stream
+    #pragma unroll 1
     for (int b = ctid; b < (H >> 5); b += ncons) {
       const uint4* src = reinterpret_cast<const uint4*>(p.x) + 4 * b;
       const uint4 v[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3)};
@@ -412,6 +415,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     RingPos rg(SG);
     int gi = 0;
     bool ok = true;
+    #pragma unroll 1
     for (; gw.valid; gw.next(), rg.next(), ++gi) {
       if (lane == 0 && gi >= SG) ok = mbar_wait(&empty_g[rg.slot], rg.phase ^ 1u, p.err);
       ok = __shfl_sync(kFull, ok, 0);
@@ -437,6 +441,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     dw.begin(nU, p);
     uint32_t dphase = 0;
     int dgroups = 0;
+    #pragma unroll 1
     for (; ok && dw.valid; dw.next(), dphase ^= 1u, ++dgroups) {
       if (lane == 0 && dgroups > 0) ok = mbar_wait(empty_d, dphase ^ 1u, p.err);
       ok = __shfl_sync(kFull, ok, 0);
@@ -444,6 +449,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
       // two tensor copies per expert: RC rows of codes and their scales (full
       // boxes: rows of the next chunk, or zeros past H, are never read)
       if (lane == 0) mbar_expect_tx(full_d, (uint32_t)p.RC * (I + nbI) * dw.ng);
+      #pragma unroll 1
       for (int ui = 0; ui < dw.ng; ++ui) {
         const int e = s.expert(dw.u0 + ui);   // warp-collective
         if (lane == 0) {
@@ -478,10 +484,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     gw.begin(nU, p);
     float ag = 0.f, au = 0.f;
     const int nbk = KC >> 5;                      // blocks per row per stage
+    #pragma unroll 1
     for (; gw.valid; gw.next(), rg.next()) {
       if (!dead) dead = !mbar_wait(&full_g[rg.slot], rg.phase, p.err);
       if (warp < gw.nn && !dead) {
         const uint8_t* base = ring_g + (size_t)rg.slot * p.slot_g;
+        #pragma unroll 1
         for (int bl = lane; bl < nbk; bl += 32) {
           const int b = gw.kc * nbk + bl;         // block of the H row
           const uint8_t* act = xs + 64 * b;
@@ -536,7 +544,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
       }
     }
   }
-  // the slot of the last gate/up stage holds the staged h
+  // staged h: in the slot of the last gate/up stage (or a region of its own)
   const int s_last = (rg.slot + SG - 1) % SG;
   uint8_t* hs = L.hs_own >= 0 ? smem + L.hs_own : ring_g + (size_t)s_last * p.slot_g;
   float* hf = reinterpret_cast<float*>(hs + L.hf_off);
@@ -547,6 +555,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   if (ctid == 0 && !grid_barrier(p.bar_ctr, *bar_target, p.err)) dead = true;
   named_sync(1, ncons);
   // h of each unique expert -> f16 blocks (read through L2: other CTAs wrote it)
+  #pragma unroll 1
   for (int t = ctid; t < nU * nbI; t += ncons) {
     const int u = t / nbI, b = t - u * nbI;
     const uint4* src = reinterpret_cast<const uint4*>(p.h + (size_t)jz[u] * I) + 4 * b;
@@ -569,6 +578,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
         // item t: expert ui = t / nbI of the group, block b = t % nbI
         int ui = 0, b = lane;
         while (b >= nbI) { b -= nbI; ++ui; }
+#pragma unroll 1
         for (int t = lane; t < n_items; t += 64) {
           // this item and the one 32 further on
           int ui2 = ui, b2 = b + 32;
