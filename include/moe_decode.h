@@ -84,10 +84,10 @@ typedef struct moe_decode* moe_decode_t;
  *   s_down    device uint8 [E, H, I/32] UE8M0 scale codes
  * w_gateup and w_down must be 32-byte aligned (rows are then 32-byte aligned
  * too); the scale arrays need no alignment (16-byte aligned scale arrays
- * enable the one-launch single-token layer). Allocates 16 bytes of device
- * state (the error word and a grid-barrier counter) and, when max_T > 0, the
- * staging buffers of moe_decode_forward_host. *out receives the handle; on
- * error *out is NULL.
+ * enable the one-launch single-token layer). Allocates 32 bytes of device
+ * state (the error word and the one-launch kernel's launch and grid-barrier
+ * counters) and, when max_T > 0, the staging buffers of
+ * moe_decode_forward_host. *out receives the handle; on error *out is NULL.
  */
 moe_status_t moe_decode_create(const moe_decode_config_t* cfg,
                                const uint8_t* w_gateup, const uint8_t* s_gateup,
@@ -159,10 +159,11 @@ moe_status_t moe_down(moe_decode_t handle, int32_t T, const uint16_t* h,
  * [T, k, I] bf16 buffer (32-byte aligned).
  * With T = 1, when moe_decode_fused_layer(handle) is 1, both projections run
  * as one cooperative launch of one CTA per SM (kernel moe_layer_fused_t1): a
- * producer warp streams the CTA's gate/up and then down weight rows with TMA,
- * and the CTAs meet at a grid barrier (a bounded wait; on timeout it sets
- * MOE_DEVICE_TIMEOUT) once h is written. Such calls on one handle must not
- * run concurrently.
+ * producer warp streams the CTA's gate/up rows and then its down rows with
+ * TMA tensor copies, fifteen consumer warps compute, and the CTAs meet at a
+ * grid barrier (a bounded wait; on timeout it sets MOE_DEVICE_TIMEOUT) once h
+ * is written. h is still written to the caller's buffer. Such calls on one
+ * handle must not run concurrently (they share the handle's counters).
  */
 moe_status_t moe_decode_layer(moe_decode_t handle, int32_t T, const uint16_t* x,
                               const int32_t* topk_ids, const float* topk_w,
