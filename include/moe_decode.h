@@ -205,6 +205,19 @@ int32_t moe_decode_version(void);
 int32_t moe_decode_fused_layer(moe_decode_t handle);
 
 /*
+ * Test support for failure detection (the pages have no counterpart): moves
+ * this handle's launch counter far ahead of its grid-barrier counter, so that
+ * the next one-launch call's grid barrier can never be met. Every CTA's
+ * bounded wait then gives up (after a few seconds), sets MOE_DEVICE_TIMEOUT
+ * and the launch completes with unspecified y; moe_decode_get_error reports
+ * it and, on a timeout, sets both counters back to zero, so later calls run
+ * normally. Nothing faults or hangs. Enqueued on the default stream and
+ * synchronised; returns MOE_ERR_INVALID_ARG for NULL, MOE_ERR_UNSUPPORTED_SHAPE
+ * when the handle does not use the one-launch form.
+ */
+moe_status_t moe_decode_arm_barrier_timeout(moe_decode_t handle);
+
+/*
  * The whole layer without any device allocation. The pages have no
  * counterpart: this entry point exists for callers that cannot call
  * cudaMalloc, such as code that runs inside another framework's memory

@@ -14,6 +14,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_decode.so")
 
 MOE_OK = 0
 MOE_DEVICE_BAD_ID = 0x1
+MOE_DEVICE_TIMEOUT = 0x2
 MOE_FLAG_NO_PDL = 0x1
 MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -57,6 +58,7 @@ SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [_st]),
     "moe_decode_version": (_i32, []),
     "moe_decode_fused_layer": (_i32, [_p]),
+    "moe_decode_arm_barrier_timeout": (_st, [_p]),
     "moe_decode_layer_noalloc": (_st, [ctypes.POINTER(MoEConfig), _p, _p, _p, _p, _i32, _p, _p, _p,
                                        _p, _p]),
 }

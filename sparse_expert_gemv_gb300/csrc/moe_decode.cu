@@ -551,7 +551,10 @@ moe_status_t moe_decode_get_error(moe_decode_t m, uint32_t* device_flags) {
   uint32_t v = 0;
   if (cudaDeviceSynchronize() != cudaSuccess ||
       cudaMemcpy(&v, m->d_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemset(m->d_err, 0, sizeof(v)) != cudaSuccess)
+      cudaMemset(m->d_err, 0, sizeof(v)) != cudaSuccess ||
+      // a grid barrier that gave up may have left the launch and barrier
+      // counters out of step: start both again from zero
+      ((v & moe::kDeviceTimeout) && cudaMemset(m->d_bar, 0, 16) != cudaSuccess))
     return MOE_ERR_CUDA;
   *device_flags = v;
   return v ? MOE_ERR_DEVICE_FAULT : MOE_OK;
@@ -572,6 +575,15 @@ const char* moe_status_string(moe_status_t status) {
 int32_t moe_decode_version(void) { return kVersion; }
 
 int32_t moe_decode_fused_layer(moe_decode_t m) { return m ? (m->fused_ok ? 1 : 0) : -1; }
+
+moe_status_t moe_decode_arm_barrier_timeout(moe_decode_t m) {
+  if (!m) return MOE_ERR_INVALID_ARG;
+  if (!m->fused_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
+  // 0x0101...01: a launch index no barrier count of this handle can reach
+  if (cudaMemset(m->d_bar, 0x01, 8) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
 
 }  // extern "C"
 

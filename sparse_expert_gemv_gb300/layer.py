@@ -82,6 +82,11 @@ class MoEDecode:
         """True when one-token layer calls run as one persistent launch."""
         return lib.moe_decode_fused_layer(self._h) == 1
 
+    def arm_barrier_timeout(self) -> None:
+        """Test support: the next one-launch call's grid barrier times out
+        (bounded; it sets MOE_DEVICE_TIMEOUT, which get_error reports)."""
+        check(lib.moe_decode_arm_barrier_timeout(self._h), "moe_decode_arm_barrier_timeout")
+
     def _dev(self, shape, dtype, out, name):
         if out is None:
             return torch.empty(shape, dtype=dtype, device=self._weights[0].device)

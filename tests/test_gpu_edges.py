@@ -280,3 +280,26 @@ def test_single_token_layer_graph_replays(dev):
         torch.cuda.synchronize()
         assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
     assert s.layer.get_error() == 0
+
+
+def test_single_token_layer_barrier_timeout_is_reported(dev):
+    # failure detection without a fault: the grid barrier's bounded wait runs
+    # out (the launch counter is moved out of its reach), every CTA gives up
+    # after its bound, the launch completes and the handle reports
+    # MOE_DEVICE_TIMEOUT; reading the error resets the counters and the next
+    # call is correct again
+    from sparse_expert_gemv_gb300 import MOE_DEVICE_TIMEOUT
+    s = Small(dev, 16, 4, 1024, 256, 1, seed=21)
+    assert s.layer.fused_single_token
+    r = s.ref()
+    _, y = _layer_once(s)
+    assert_within(tensor_to_f64(y), r["y_spec"], tol_y(r["y_spec"]), "y before")
+    assert s.layer.get_error() == 0
+    s.layer.arm_barrier_timeout()
+    _layer_once(s)                                   # y unspecified
+    assert s.layer.get_error() == MOE_DEVICE_TIMEOUT
+    assert s.layer.get_error() == 0                  # reading clears it
+    for _ in range(3):
+        _, y = _layer_once(s)
+        assert_within(tensor_to_f64(y), r["y_spec"], tol_y(r["y_spec"]), "y after")
+    assert s.layer.get_error() == 0

@@ -31,9 +31,11 @@ def _layer(case: Case, dev, **kw):
     return MoEDecode(*device_weights(w, case.experts, dev), k=w.k, max_T=max(case.T, 1), **kw)
 
 
-def _run_and_check(case: Case, dev, rows=None):
+def _run_and_check(case: Case, dev, rows=None, expect_fused=None):
     w = case.w
     layer = _layer(case, dev)
+    if expect_fused is not None:
+        assert layer.fused_single_token == expect_fused
     x = bf16_tensor(case.x_bits, dev)
     ids = torch.from_numpy(case.ids).to(dev)
     tw = torch.from_numpy(case.tw).to(dev)
@@ -45,7 +47,11 @@ def _run_and_check(case: Case, dev, rows=None):
     S = case.tokens
     hm = assert_within(tensor_to_f64(h)[S], ref["h_spec"][S], tol_h(ref["h_spec"][S]), "h")
     ym = assert_within(tensor_to_f64(y)[S], ref["y_spec"][S], tol_y(ref["y_spec"][S]), "y")
-    assert torch.equal(y.view(torch.int16)[S], y2.view(torch.int16)[S]), "layer() differs from gate_up+down"
+    if case.T == 1 and layer.fused_single_token:
+        # one launch for both projections: its own sums, checked on their own
+        assert_within(tensor_to_f64(y2)[S], ref["y_spec"][S], tol_y(ref["y_spec"][S]), "y (one launch)")
+    else:
+        assert torch.equal(y.view(torch.int16)[S], y2.view(torch.int16)[S]), "layer() differs from gate_up+down"
     pure = metrics(tensor_to_f64(y)[S], ref["y_pure"][S])
     assert layer.get_error() == 0
     layer.close()
@@ -54,7 +60,9 @@ def _run_and_check(case: Case, dev, rows=None):
 
 @pytest.mark.parametrize("c", [0, 1, 2, 3])
 def test_workload_parity_full(c, dev):
-    hm, ym, pure = _run_and_check(Case(c), dev)
+    # the batch-1 decode workload (1) is the one-launch path's case, as timed
+    # by the bench; the tiny layer (0) has H below that kernel's minimum
+    hm, ym, pure = _run_and_check(Case(c), dev, expect_fused={0: False, 1: True}.get(c))
     print(f"workload {c}: h {hm}  y {ym}  y vs fp64-exact {pure}")
     assert ym["cosine"] > 0.9999
 
