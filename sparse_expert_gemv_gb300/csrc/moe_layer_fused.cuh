@@ -245,42 +245,47 @@ __device__ __forceinline__ float dot_block(const uint8_t* codes, const uint8_t* 
   return (p + q) + (r + s);
 }
 
-// The CTA's gate/up stage sequence: up to 15 neurons of one expert over a
-// K-chunk (u-major over the unique experts). Producer and consumers run the
-// same warp-uniform walk; it steps without divisions.
+// The CTA's gate/up stage sequence. The grid is split into one group of
+// CTAs per unique expert (gridDim.x >= nU; group sizes differ by at most one)
+// and each CTA of a group takes an equal share of that expert's I neurons,
+// so no CTA's share straddles two experts; the share is cut into stages of
+// 15 neurons (the remainder last), each over K-chunks of KC codes.
+// Producer and consumers run the same warp-uniform walk.
 struct GuWalk {
-  int g, g1;          // neuron cursor and end of the CTA's slice
-  int u, i0, nn, kc, nkc, I;
+  int u, i0, nn, kc, nkc;
+  int i_beg, n, nst, st;   // the CTA's share [i_beg, i_beg + n), in nst stages
   bool valid;
 
-  __device__ __forceinline__ void set_nn() {
-    valid = g < g1;
-    nn = kFusedNeurons;
-    if (nn > I - i0) nn = I - i0;
-    if (nn > g1 - g) nn = g1 - g;
+  __device__ __forceinline__ void set_stage() {
+    valid = st < nst;
+    if (!valid) return;
+    // full 15-neuron stages, the remainder last (a stage's TMA box is 15 rows
+    // whatever its size, so equal smaller stages would fetch overlapping rows)
+    i0 = i_beg + st * kFusedNeurons;
+    nn = n - st * kFusedNeurons < kFusedNeurons ? n - st * kFusedNeurons : kFusedNeurons;
   }
   __device__ __forceinline__ void begin(int nU, const FusedParams& p) {
-    I = p.I;
     nkc = p.H / p.KC;
-    // 32-bit: nU * I * gridDim.x stays far below 2^32 for every supported shape
-    const uint32_t G = (uint32_t)nU * (uint32_t)I;
-    g = (int)(G * blockIdx.x / gridDim.x);
-    g1 = (int)(G * (blockIdx.x + 1) / gridDim.x);
-    u = g / I;
-    i0 = g - u * I;
     kc = 0;
-    set_nn();
+    st = 0;
+    nst = 0;
+    valid = false;
+    if (nU <= 0) return;
+    const uint32_t G = gridDim.x, bx = blockIdx.x;
+    u = (int)(bx * (uint32_t)nU / G);
+    const uint32_t lo = ((uint32_t)u * G + nU - 1) / nU;         // first CTA of group u
+    const uint32_t hi = ((uint32_t)(u + 1) * G + nU - 1) / nU;   // one past its last
+    const uint32_t c = hi - lo, r = bx - lo;
+    i_beg = (int)((uint32_t)p.I * r / c);
+    n = (int)((uint32_t)p.I * (r + 1) / c) - i_beg;
+    nst = (n + kFusedNeurons - 1) / kFusedNeurons;
+    set_stage();
   }
   __device__ __forceinline__ void next() {
     if (++kc < nkc) return;
     kc = 0;
-    g += nn;
-    i0 += nn;
-    if (i0 == I) {
-      i0 = 0;
-      ++u;
-    }
-    set_nn();
+    ++st;
+    set_stage();
   }
   __device__ __forceinline__ bool last_kc() const { return kc == nkc - 1; }
 };
