@@ -115,40 +115,47 @@ int gcd_int(int a, int b) { return b ? gcd_int(b, a % b) : a; }
 
 // Ring geometry of moe_layer_fused_t1 for this handle's shape; false when the
 // shape or the pointers do not suit it (the two-kernel path is used instead).
+// The ring carries the CTA's gate/up tiles and then its down row groups, as
+// many slots as fit beside the staged x and h.
 bool plan_fused(const moe_decode* m, moe::FusedParams& fp, size_t& smem) {
   const moe_decode_config_t& c = m->cfg;
   if (!m->fused_ok || c.H % 512 || c.I % 128 || !aligned(m->sgu, 16) || !aligned(m->sd, 16))
     return false;
-  // a stage's K-chunk: whole 2 KB rows when H allows, else 1 KB or 512 B
-  const int KC = (c.H % 2048 == 0) ? 2048 : (c.H % 1024 == 0) ? 1024 : 512;
-  const int slot_g = moe::GuStageLayout(KC).end;        // a multiple of 128
   const int nbI = c.I / 32;
   const int RG = 16 / gcd_int(16, nbI);
   if (c.H % RG) return false;
   const int rows_cta = (c.H / RG + m->num_sms - 1) / m->num_sms * RG;
-  const int RC = std::min(rows_cta, moe::kFusedConsumers / RG * RG);
-  if (RC < RG) return false;
-  const int slot_d = moe::round128(RC * (c.I + nbI));
-  auto bytes = [&](int SG, int SD) {
-    return (size_t)moe::FusedSmem(SG, slot_g, SD, slot_d, c.H, c.I, c.k).total;
-  };
-  // two gate/up slots (up to ~125 KB of tiles in flight per SM), then the
-  // down group buffer as large as fits (every routed expert's row chunk when
-  // it can), then any room left goes back to the gate/up ring
-  int SG = 2, SD = c.k;
-  while (SD > 1 && bytes(SG, SD) > m->smem_per_block) --SD;
-  if (bytes(SG, SD) > m->smem_per_block) return false;
-  while (SG < 8 && bytes(SG + 1, SD) <= m->smem_per_block) ++SG;
-  smem = bytes(SG, SD);
-  fp.KC = KC;
-  fp.kin = std::min(256, KC / 4);
-  fp.SG = SG;
-  fp.slot_g = slot_g;
-  fp.SD = SD;
-  fp.slot_d = slot_d;
-  fp.RG = RG;
-  fp.RC = RC;
-  return true;
+  constexpr int kMaxSlots = 16;
+  // a stage's K-chunk: the first of these that H allows and the ring holds
+  // (1024-code stages put the first tiles to work sooner than whole 2 KB rows
+  // and free ring slots for the down rows earlier)
+  for (const int KC : {1024, 2048, 512}) {
+    if (c.H % KC) continue;
+    const int slot_g = moe::GuStageLayout(KC).end;        // a multiple of 128
+    // down row chunks of RC rows, as many as the consumers cover and a slot holds
+    int RC = std::min(rows_cta, moe::kFusedConsumers / RG * RG);
+    while (RC >= RG && moe::round128(RC * (c.I + nbI)) > slot_g) RC -= RG;
+    if (RC < RG) continue;
+    const int slot_d = moe::round128(RC * (c.I + nbI));
+    const int SR = slot_g / slot_d;
+    auto bytes = [&](int SG) { return (size_t)moe::FusedSmem(SG, slot_g, c.H, c.I, c.k).total; };
+    if (bytes(2) > m->smem_per_block) continue;
+    int SG = 2;
+    while (SG < kMaxSlots && bytes(SG + 1) <= m->smem_per_block) ++SG;
+    // every group of a row chunk is resident at once
+    if ((c.k + SR - 1) / SR > SG) continue;
+    smem = bytes(SG);
+    fp.KC = KC;
+    fp.kin = std::min(256, KC / 4);
+    fp.SG = SG;
+    fp.slot_g = slot_g;
+    fp.SR = SR;
+    fp.slot_d = slot_d;
+    fp.RG = RG;
+    fp.RC = RC;
+    return true;
+  }
+  return false;
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once (no link to libcuda).

@@ -7,22 +7,23 @@
 // up dot products itself; in the down phase a warp owns one output row.
 //
 // What the single launch adds is the memory stream. One producer warp per CTA
-// streams, with TMA, first the CTA's gate/up rows (tiles of fifteen neurons'
-// gate and up rows over a K-chunk, into a ring of SG shared-memory slots
-// guarded by mbarriers), then, right after the last gate/up tile, its down
-// rows for every routed expert into a buffer of their own, so HBM keeps
-// streaming while the consumers compute and the down rows land while h is
-// being exchanged. h itself is staged in the slot of the last gate/up stage
-// (or in its own region when it does not fit there).
+// streams, with TMA, everything the CTA reads through one ring of SG
+// shared-memory slots guarded by mbarriers: first its gate/up tiles (fifteen
+// neurons' gate and up rows over a K-chunk), then its down rows for every
+// routed expert, in groups of whole slots, each group issued as soon as a
+// gate/up stage has freed its slot. HBM so keeps streaming while the
+// consumers compute, and the down rows land before h has been exchanged. h
+// itself is staged in a region of its own.
 //
 // Every CTA needs every h value, so the CTAs meet at a grid barrier between
 // the phases (the launch is cooperative, so all of them are resident). Each
 // CTA learns the launch's index from one counter add at its start; at the
-// barrier it then only posts a release add to a second counter and polls it
-// (acquire loads) for the value that index implies, one round trip less than
-// a barrier that must read back its own arrival. (Publishing h as
-// epoch-tagged words that readers poll directly measured slower on this
-// part: every CTA polling all of h floods L2 while the down rows stream.)
+// barrier it then only posts a release add to a second counter and, after
+// preparing its down work (where each item's rows sit, the arrival of its
+// down groups), polls it (acquire loads) for the value that index implies.
+// (Publishing h as epoch-tagged words that readers poll directly measured
+// slower on this part: every CTA polling all of h floods L2 while the down
+// rows stream.)
 //
 // Arithmetic. Each lane reduces one 32-element MX block at a time: 32 E4M3
 // codes against 32 activations, FP32 accumulation, then the block's UE8M0
@@ -76,8 +77,8 @@ struct FusedParams {
   int kin;      // uint32 words per innermost box row of tm_codes (KC/4 or 256)
   int SG;       // gate/up ring slots
   int slot_g;   // bytes per gate/up slot (GuStageLayout(KC).end)
-  int SD;       // routed experts per down group (one row chunk each)
-  int slot_d;   // bytes per expert in a down group: RC rows of codes, then RC rows of scales
+  int SR;       // down row chunks per ring slot (one routed expert's RC rows each)
+  int slot_d;   // bytes per down chunk in a slot: RC rows of codes, then RC rows of scales
   int RG;       // down row granule (keeps scale copies 16-byte aligned)
   int RC;       // down rows per chunk (multiple of RG, <= kFusedConsumers)
 };
@@ -97,26 +98,23 @@ struct GuStageLayout {
 };
 
 // Shared-memory map of the kernel (byte offsets, each 128-byte aligned). The
-// SG ring slots start at 0; the staged h reuses one of them when it fits.
+// SG ring slots start at 0.
 struct FusedSmem {
-  int dg;       // the down group buffer: SD experts x slot_d bytes
   int xs;       // x as f16, [H/32] blocks of 64 bytes (swizzled 16-byte chunks)
   int xf;       // [H/32] FP32 block factors 2^-e of x
   int ep;       // the value bar_ctr reaches when this launch's CTAs have all arrived
   int cf;       // [k] combined routing weight of each unique expert
   int jz;       // [k] first slot j routed to each unique expert
-  int db;       // [32] byte offset of each expert of a down group
-  int bars;     // mbarriers: full_g[SG], empty_g[SG], full_d, empty_d
+  int bars;     // mbarriers: full[SG], empty[SG]
   int words;    // 16 warps x 32 words of expert bitmap
-  // h of each unique expert as f16 ([k][I/32] blocks of 64 bytes), then its
-  // FP32 block factors: at hs_off inside a ring slot when h_bytes <= slot_g,
-  // else at hs_own (a region of its own)
-  int hf_off, h_bytes, hs_own;
+  // h of each unique expert as f16 ([k][I/32] blocks of 64 bytes); then, per
+  // down item t (block t % (I/32) of unique expert t / (I/32)), its FP32
+  // factor (routing weight x block factor) and the shared-memory offsets of
+  // its codes and scales in the current row chunk (row 0)
+  int hs, tf, tc, ts;
   int total;
-  __host__ __device__ FusedSmem(int SG, int slot_g, int SD, int slot_d, int H, int I, int k) {
+  __host__ __device__ FusedSmem(int SG, int slot_g, int H, int I, int k) {
     int o = SG * slot_g;
-    dg = o;
-    o += SD * slot_d;
     xs = o;
     o += round128(H * 2);
     xf = o;
@@ -127,19 +125,18 @@ struct FusedSmem {
     o += round128(k * 4);
     jz = o;
     o += round128(k * 4);
-    db = o;
-    o += 128;
     bars = o;
-    o += round128((2 * SG + 2) * 8);
+    o += round128(2 * SG * 8);
     words = o;
     o += 16 * 32 * 4;
-    hf_off = round128(k * I * 2);
-    h_bytes = hf_off + round128(k * (I >> 5) * 4);
-    hs_own = -1;
-    if (h_bytes > slot_g) {
-      hs_own = o;
-      o += h_bytes;
-    }
+    hs = o;
+    o += round128(k * I * 2);
+    tf = o;
+    o += round128(k * (I >> 5) * 4);
+    tc = o;
+    o += round128(k * (I >> 5) * 4);
+    ts = o;
+    o += round128(k * (I >> 5) * 4);
     total = o;
   }
 };
@@ -291,10 +288,10 @@ struct GuWalk {
 };
 
 // The CTA's down work: output rows [r0, r1) (whole granules of RG rows), cut
-// in chunks of RC rows; each chunk's unique experts in groups of up to SD
-// (one expert per down slot). A group is loaded and consumed as one unit.
+// in chunks of RC rows; each chunk's unique experts in groups of up to SR,
+// one group per ring slot.
 struct DownWalk {
-  int r0, r1, c0, rc, u0, ng, nU, RC, SD;
+  int r0, r1, c0, rc, u0, ng, nU, RC, SR;
   bool valid;
 
   __device__ __forceinline__ void begin(int nU_, const FusedParams& p) {
@@ -303,12 +300,12 @@ struct DownWalk {
     r1 = (int)(nrg * (blockIdx.x + 1) / gridDim.x) * p.RG;
     nU = nU_;
     RC = p.RC;
-    SD = p.SD;
+    SR = p.SR;
     c0 = r0;
     u0 = 0;
     valid = r0 < r1 && nU > 0;
     rc = (r1 - c0) < RC ? (r1 - c0) : RC;
-    ng = nU < SD ? nU : SD;
+    ng = nU < SR ? nU : SR;
   }
   __device__ __forceinline__ void next() {
     u0 += ng;
@@ -318,7 +315,7 @@ struct DownWalk {
       valid = c0 < r1;
       rc = (r1 - c0) < RC ? (r1 - c0) : RC;
     }
-    ng = (nU - u0) < SD ? (nU - u0) : SD;
+    ng = (nU - u0) < SR ? (nU - u0) : SR;
   }
   __device__ __forceinline__ bool last_group() const { return u0 + ng >= nU; }
 };
@@ -336,12 +333,16 @@ struct RingPos {
   }
 };
 
-// Grid barrier of a cooperative launch, called by one thread per CTA after the
-// CTA's threads have met: a release add of one arrival (cumulative over what
-// those threads wrote), then bounded acquire polls until all arrived.
-__device__ __forceinline__ bool grid_barrier(unsigned long long* bar, unsigned long long target,
-                                             uint32_t* err) {
+// Grid barrier of a cooperative launch, in two halves used by one thread per
+// CTA. Arrival, after the CTA's threads have met at a named barrier: a release
+// add of one (cumulative over what those threads wrote). Wait: bounded acquire
+// polls until the count reaches this launch's target; false after a timeout
+// (with the error flag set).
+__device__ __forceinline__ void grid_arrive(unsigned long long* bar) {
   asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar) : "memory");
+}
+__device__ __forceinline__ bool grid_wait(const unsigned long long* bar, unsigned long long target,
+                                          uint32_t* err) {
 #pragma unroll 1
   for (uint32_t it = 0; it < kWaitLimit; ++it) {
     unsigned long long v;
@@ -357,18 +358,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = p.H, I = p.I, KC = p.KC, SG = p.SG, nbI = I >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const FusedSmem L(SG, p.slot_g, p.SD, p.slot_d, H, I, p.k);
+  const FusedSmem L(SG, p.slot_g, H, I, p.k);
   uint8_t* ring_g = smem;
   uint8_t* xs = smem + L.xs;
   float* xf = reinterpret_cast<float*>(smem + L.xf);
-  int* db = reinterpret_cast<int*>(smem + L.db);
   unsigned long long* bar_target = reinterpret_cast<unsigned long long*>(smem + L.ep);
   float* cf = reinterpret_cast<float*>(smem + L.cf);
   int* jz = reinterpret_cast<int*>(smem + L.jz);
   uint64_t* full_g = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty_g = full_g + SG;
-  uint64_t* full_d = empty_g + SG;    // one barrier pair for the down group buffer
-  uint64_t* empty_d = full_d + 1;
   uint32_t* sm_words = reinterpret_cast<uint32_t*>(smem + L.words);
   const int ctid = threadIdx.x;                    // consumer thread index
   const int ncons = kFusedConsumers * 32;
@@ -384,8 +382,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
       mbar_init(&full_g[i], 1);
       mbar_init(&empty_g[i], kFusedConsumers);
     }
-    mbar_init(full_d, 1);
-    mbar_init(empty_d, kFusedConsumers);
     mbar_init_fence();
   }
   __syncthreads();
@@ -415,53 +411,51 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
 
   if (warp == kFusedConsumers) {
     // ------------------------------------------------------------ producer
+    // one ring for everything the CTA streams: its gate/up tiles, then its
+    // down row groups, each into the next slot as soon as it is free
     GuWalk gw;
     gw.begin(nU, p);
+    DownWalk dw;
+    dw.begin(nU, p);
     RingPos rg(SG);
     int gi = 0;
     bool ok = true;
     #pragma unroll 1
-    for (; gw.valid; gw.next(), rg.next(), ++gi) {
+    for (; gw.valid || dw.valid; rg.next(), ++gi) {
       if (lane == 0 && gi >= SG) ok = mbar_wait(&empty_g[rg.slot], rg.phase ^ 1u, p.err);
       ok = __shfl_sync(kFull, ok, 0);
       if (!ok) break;
-      const int e = s.expert(gw.u);   // warp-collective
-      if (lane == 0) {
-        uint8_t* dst = ring_g + (size_t)rg.slot * p.slot_g;
-        uint64_t* bar = &full_g[rg.slot];
-        // four tensor copies: the stage's gate rows, up rows, and their scales
-        // (full boxes; rows past the expert are never read)
-        mbar_expect_tx(bar, 2u * kFusedNeurons * KC + 2u * kFusedNeurons * (KC >> 5));
-        const int row = e * 2 * I + gw.i0;
-        const int kchunk = gw.kc * ((KC >> 2) / p.kin);
-        tma_load_3d(dst, &p.tm_codes, 0, kchunk, row, bar);
-        tma_load_3d(dst + lay.up, &p.tm_codes, 0, kchunk, row + I, bar);
-        tma_load_2d(dst + lay.gs, &p.tm_scales, gw.kc * (KC >> 7), row, bar);
-        tma_load_2d(dst + lay.us, &p.tm_scales, gw.kc * (KC >> 7), row + I, bar);
-      }
-    }
-    // down groups, right behind the last gate/up tile (the first group's
-    // buffer is free; each later one waits for the previous to be consumed)
-    DownWalk dw;
-    dw.begin(nU, p);
-    uint32_t dphase = 0;
-    int dgroups = 0;
-    #pragma unroll 1
-    for (; ok && dw.valid; dw.next(), dphase ^= 1u, ++dgroups) {
-      if (lane == 0 && dgroups > 0) ok = mbar_wait(empty_d, dphase ^ 1u, p.err);
-      ok = __shfl_sync(kFull, ok, 0);
-      if (!ok) break;
-      // two tensor copies per expert: RC rows of codes and their scales (full
-      // boxes: rows of the next chunk, or zeros past H, are never read)
-      if (lane == 0) mbar_expect_tx(full_d, (uint32_t)p.RC * (I + nbI) * dw.ng);
-      #pragma unroll 1
-      for (int ui = 0; ui < dw.ng; ++ui) {
-        const int e = s.expert(dw.u0 + ui);   // warp-collective
+      uint8_t* dst = ring_g + (size_t)rg.slot * p.slot_g;
+      uint64_t* bar = &full_g[rg.slot];
+      if (gw.valid) {
+        const int e = s.expert(gw.u);   // warp-collective
         if (lane == 0) {
-          uint8_t* dst = smem + L.dg + (size_t)ui * p.slot_d;
-          tma_load_4d(dst, &p.tm_dcodes, 0, 0, dw.c0, e, full_d);
-          tma_load_2d(dst + (size_t)p.RC * I, &p.tm_dscales, dw.c0 * (nbI >> 2), e, full_d);
+          // four tensor copies: the stage's gate rows, up rows, and their
+          // scales (full boxes; rows past the expert are never read)
+          mbar_expect_tx(bar, 2u * kFusedNeurons * KC + 2u * kFusedNeurons * (KC >> 5));
+          const int row = e * 2 * I + gw.i0;
+          const int kchunk = gw.kc * ((KC >> 2) / p.kin);
+          tma_load_3d(dst, &p.tm_codes, 0, kchunk, row, bar);
+          tma_load_3d(dst + lay.up, &p.tm_codes, 0, kchunk, row + I, bar);
+          tma_load_2d(dst + lay.gs, &p.tm_scales, gw.kc * (KC >> 7), row, bar);
+          tma_load_2d(dst + lay.us, &p.tm_scales, gw.kc * (KC >> 7), row + I, bar);
         }
+        gw.next();
+      } else {
+        // a down group: two tensor copies per expert, RC rows of codes and
+        // their scales (full boxes: rows of the next chunk, or zeros past H,
+        // are never read)
+        if (lane == 0) mbar_expect_tx(bar, (uint32_t)p.RC * (I + nbI) * dw.ng);
+        #pragma unroll 1
+        for (int ui = 0; ui < dw.ng; ++ui) {
+          const int e = s.expert(dw.u0 + ui);   // warp-collective
+          if (lane == 0) {
+            uint8_t* d = dst + (size_t)ui * p.slot_d;
+            tma_load_4d(d, &p.tm_dcodes, 0, 0, dw.c0, e, bar);
+            tma_load_2d(d + (size_t)p.RC * I, &p.tm_dscales, dw.c0 * (nbI >> 2), e, bar);
+          }
+        }
+        dw.next();
       }
     }
     // never leave with copies in flight
@@ -469,13 +463,42 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
       RingPos r(SG);
       for (int d = 0; d < gi; ++d, r.next())
         if (d >= gi - SG) mbar_wait(&full_g[r.slot], r.phase, p.err);
-      if (dgroups > 0) mbar_wait(full_d, dphase ^ 1u, p.err);
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
   named_sync(1, ncons);   // x staged
+
+  if (warp == 0) {
+    // while the first tiles are in flight: per unique expert u (lane u), the
+    // combined routing weight of its slots and the first slot routed to it
+    // (its h row); out-of-range ids give h = 0 (written by CTA 0) and no down
+    // term
+    const int e = s.expert_per_lane(lane);
+    uint32_t jm = 0;
+    float c = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      const int idj = __shfl_sync(kFull, s.id[j], 0);    // lane 0 holds the token
+      const float wjj = __shfl_sync(kFull, wj, j);
+      if (j < p.k && idj == e) {
+        jm |= 1u << j;
+        c += wjj;
+      }
+    }
+    if (lane < nU) {
+      cf[lane] = c;
+      jz[lane] = __ffs(jm) - 1;
+    }
+    if (blockIdx.x == 0) {
+      const uint32_t bad = __shfl_sync(kFull, s.badmask, 0);
+      for (uint32_t m = bad; m; m &= m - 1) {
+        uint16_t* row = p.h + (size_t)(__ffs(m) - 1) * I;
+        for (int i = lane; i < I; i += 32) row[i] = 0;
+      }
+    }
+  }
 
   const LaneBlock lb(lane);
   // a warp whose bounded wait gave up stops waiting and computing but still
@@ -521,97 +544,98 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     }
   }
 
-  if (warp == 0) {
-    // per unique expert u (lane u): the combined routing weight of its slots
-    // and the first slot routed to it (its h row); out-of-range ids give h = 0
-    // (written by CTA 0) and no down term
-    const int e = s.expert_per_lane(lane);
-    uint32_t jm = 0;
-    float c = 0.f;
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      const int idj = __shfl_sync(kFull, s.id[j], 0);    // lane 0 holds the token
-      const float wjj = __shfl_sync(kFull, wj, j);
-      if (j < p.k && idj == e) {
-        jm |= 1u << j;
-        c += wjj;
-      }
+  uint8_t* hs = smem + L.hs;
+  float* tf = reinterpret_cast<float*>(smem + L.tf);
+  int* tc = reinterpret_cast<int*>(smem + L.tc);
+  int* ts = reinterpret_cast<int*>(smem + L.ts);
+
+  // ---- down, one row chunk at a time: its groups sit in the ring slots
+  // after the gate/up tiles; warp owns row c0 + warp and its lanes take the
+  // chunk's items (expert u, block b), two at a time
+  DownWalk dw;
+  dw.begin(nU, p);
+  const int n_items = nU * nbI;
+  int c0 = 0, rc = 0, ngr = 0;
+  RingPos pos0 = rg;
+  // The next chunk: where each item's codes and scales sit (expert u's rows
+  // are chunk u % SR of the chunk's group u / SR, at ring position
+  // pos0 + u / SR) ...
+  auto chunk_tables = [&]() {
+    c0 = dw.c0;
+    rc = dw.rc;
+    pos0 = rg;
+    #pragma unroll 1
+    for (int t = ctid; t < n_items; t += ncons) {
+      const int u = t / nbI, b = t - u * nbI;
+      const int g = u / p.SR;
+      const int slot = pos0.slot + g < SG ? pos0.slot + g : pos0.slot + g - SG;
+      const int off = slot * p.slot_g + (u - g * p.SR) * p.slot_d;
+      tc[t] = off + 32 * b;
+      ts[t] = off + p.RC * I + b;
     }
-    if (lane < nU) {
-      cf[lane] = c;
-      jz[lane] = __ffs(jm) - 1;
+  };
+  // ... and the arrival of its groups
+  auto chunk_wait = [&]() {
+    ngr = 0;
+    #pragma unroll 1
+    for (bool more = true; more; rg.next(), ++ngr) {
+      if (!dead) dead = !mbar_wait(&full_g[rg.slot], rg.phase, p.err);
+      more = !dw.last_group();
+      dw.next();
     }
-    if (blockIdx.x == 0) {
-      const uint32_t bad = __shfl_sync(kFull, s.badmask, 0);
-      for (uint32_t m = bad; m; m &= m - 1) {
-        uint16_t* row = p.h + (size_t)(__ffs(m) - 1) * I;
-        for (int i = lane; i < I; i += 32) row[i] = 0;
-      }
-    }
+  };
+  bool have = dw.valid;
+  // every h value of every CTA is written before any CTA reads h; the first
+  // chunk is prepared while the other CTAs arrive
+  named_sync(1, ncons);
+  if (ctid == 0) grid_arrive(p.bar_ctr);
+  if (have) {
+    chunk_tables();
+    chunk_wait();
   }
-  // staged h: in the slot of the last gate/up stage (or a region of its own)
-  const int s_last = (rg.slot + SG - 1) % SG;
-  uint8_t* hs = L.hs_own >= 0 ? smem + L.hs_own : ring_g + (size_t)s_last * p.slot_g;
-  float* hf = reinterpret_cast<float*>(hs + L.hf_off);
-  if (ctid < 32) db[ctid] = L.dg + ctid * p.slot_d;
-  // every h value of every CTA is written before any CTA reads h (and the
-  // last gate/up stage's slot is idle once every consumer is past it)
+  if (ctid == 0 && !grid_wait(p.bar_ctr, *bar_target, p.err)) dead = true;
   named_sync(1, ncons);
-  if (ctid == 0 && !grid_barrier(p.bar_ctr, *bar_target, p.err)) dead = true;
-  named_sync(1, ncons);
-  // h of each unique expert -> f16 blocks (read through L2: other CTAs wrote it)
+  // h of each unique expert -> f16 blocks (read through L2: other CTAs wrote
+  // it), and each block's factor times its expert's routing weight
   #pragma unroll 1
-  for (int t = ctid; t < nU * nbI; t += ncons) {
+  for (int t = ctid; t < n_items; t += ncons) {
     const int u = t / nbI, b = t - u * nbI;
     const uint4* src = reinterpret_cast<const uint4*>(p.h + (size_t)jz[u] * I) + 4 * b;
     const uint4 v[4] = {__ldcg(src), __ldcg(src + 1), __ldcg(src + 2), __ldcg(src + 3)};
-    hf[t] = stage_block_f16(v, hs + 64 * t, b);
+    tf[t] = cf[u] * stage_block_f16(v, hs + 64 * t, b);
   }
-  named_sync(1, ncons);
-
-  // ---- down: warp owns row c0 + warp of each chunk; its lanes take the
-  // group's (expert, block) pairs, two at a time
+  named_sync(1, ncons);   // h staged
   {
-    DownWalk dw;
-    dw.begin(nU, p);
-    uint32_t dphase = 0;
-    float acc = 0.f;
-    for (; dw.valid; dw.next(), dphase ^= 1u) {
-      if (!dead) dead = !mbar_wait(full_d, dphase, p.err);
-      if (warp < dw.rc && !dead) {
-        const int n_items = dw.ng * nbI;
-        // item t: expert ui = t / nbI of the group, block b = t % nbI
-        int ui = 0, b = lane;
-        while (b >= nbI) { b -= nbI; ++ui; }
+    const int wI = warp * I, wS = warp * nbI;
+    #pragma unroll 1
+    while (have) {
+      float acc = 0.f;
+      if (warp < rc && !dead) {
 #pragma unroll 1
         for (int t = lane; t < n_items; t += 64) {
-          // this item and the one 32 further on
-          int ui2 = ui, b2 = b + 32;
-          while (b2 >= nbI) { b2 -= nbI; ++ui2; }
+          // this item and the one 32 further on (the same one again past the end)
           const bool two = t + 32 < n_items;
-          const uint8_t* s1 = smem + db[ui];
-          const float d1 = dot_block(s1 + (size_t)warp * I + 32 * b, hs + (size_t)(dw.u0 + ui) * nbI * 64 + 64 * b, lb);
-          float d2 = 0.f;
-          const uint8_t* s2 = smem + db[ui2 < 32 ? ui2 : 0];
-          if (two) d2 = dot_block(s2 + (size_t)warp * I + 32 * b2, hs + (size_t)(dw.u0 + ui2) * nbI * 64 + 64 * b2, lb);
-          const float v1 = d1 * hf[(dw.u0 + ui) * nbI + b] * ue8m0_to_f32(s1[(size_t)p.RC * I + warp * nbI + b]);
-          acc = fmaf(v1, cf[dw.u0 + ui], acc);
-          if (two) {
-            const float v2 = d2 * hf[(dw.u0 + ui2) * nbI + b2] * ue8m0_to_f32(s2[(size_t)p.RC * I + warp * nbI + b2]);
-            acc = fmaf(v2, cf[dw.u0 + ui2], acc);
-          }
-          // advance both cursors by 64 items
-          ui = ui2;
-          b = b2 + 32;
-          while (b >= nbI) { b -= nbI; ++ui; }
+          const int t2 = two ? t + 32 : t;
+          const float d1 = dot_block(smem + tc[t] + wI, hs + 64 * t, lb);
+          const float d2 = dot_block(smem + tc[t2] + wI, hs + 64 * t2, lb);
+          acc = fmaf(d1 * ue8m0_to_f32(smem[ts[t] + wS]), tf[t], acc);
+          if (two) acc = fmaf(d2 * ue8m0_to_f32(smem[ts[t2] + wS]), tf[t2], acc);
         }
       }
+      const float v = warp_sum(acc);
+      if (lane == 0 && warp < rc) p.y[c0 + warp] = f32_to_bf16_rn(v);
+      // the chunk's slots are free again
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty_d);
-      if (dw.last_group()) {
-        const float v = warp_sum(acc);
-        if (lane == 0 && warp < dw.rc) p.y[dw.c0 + warp] = f32_to_bf16_rn(v);
-        acc = 0.f;
+      RingPos r = pos0;
+      for (int i = 0; i < ngr; ++i, r.next())
+        if (lane == 0) mbar_arrive(&empty_g[r.slot]);
+      have = dw.valid;
+      if (have) {
+        // every warp is past its reads of the item tables before they change
+        named_sync(1, ncons);
+        chunk_tables();
+        chunk_wait();
+        named_sync(1, ncons);
       }
     }
     if (nU == 0) {
