@@ -153,6 +153,9 @@ bool plan_fused(const moe_decode* m, moe::FusedParams& fp, size_t& smem) {
     fp.slot_d = slot_d;
     fp.RG = RG;
     fp.RC = RC;
+    fp.nkc = c.H / KC;
+    fp.kdiv = KC / (4 * fp.kin);
+    fp.nrg = c.H / RG;
     return true;
   }
   return false;

@@ -244,19 +244,34 @@ struct WarpSchedule {
 
   __device__ __forceinline__ void build(const int32_t* __restrict__ ids, int T, int k, int E,
                                         uint32_t* sm_words, uint32_t* err) {
+    load(ids, T, k);
+    finish(E, sm_words, err);
+  }
+
+  // The two halves of build(): load() only issues the id loads, so that
+  // independent work can run while they are in flight before finish().
+  __device__ __forceinline__ void load(const int32_t* __restrict__ ids, int T, int k) {
     const int lane = threadIdx.x & 31;
+    badmask = 0u;   // slots in use until finish()
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      id[j] = -1;
+      if (lane < T && j < k) {
+        id[j] = __ldg(ids + lane * k + j);
+        badmask |= 1u << j;
+      }
+    }
+  }
+  __device__ __forceinline__ void finish(int E, uint32_t* sm_words, uint32_t* err) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t used = badmask;
     badmask = 0u;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      int v = -1;
-      if (lane < T && j < k) {
-        v = __ldg(ids + lane * k + j);
-        if (v < 0 || v >= E) {
-          badmask |= 1u << j;
-          v = -1;
-        }
+      if (((used >> j) & 1u) && (id[j] < 0 || id[j] >= E)) {
+        badmask |= 1u << j;
+        id[j] = -1;
       }
-      id[j] = v;
     }
     if (badmask) atomicOr(err, kDeviceBadId);
     sm_words[lane] = 0u;

@@ -81,6 +81,9 @@ struct FusedParams {
   int slot_d;   // bytes per down chunk in a slot: RC rows of codes, then RC rows of scales
   int RG;       // down row granule (keeps scale copies 16-byte aligned)
   int RC;       // down rows per chunk (multiple of RG, <= kFusedConsumers)
+  int nkc;      // H / KC: K-chunks per gate/up row
+  int kdiv;     // KC / (4 * kin): tm_codes dim-1 boxes per K-chunk
+  int nrg;      // H / RG: down row granules
 };
 
 __host__ __device__ constexpr int round128(int v) { return (v + 127) / 128 * 128; }
@@ -253,6 +256,25 @@ struct GuWalk {
   int i_beg, n, nst, st;   // the CTA's share [i_beg, i_beg + n), in nst stages
   bool valid;
 
+  // The CTA's expert group u and share [i_beg, i_beg + n) when nU unique
+  // experts are routed. Shape and grid values only: each lane computes it
+  // for nU = lane + 1 before the routing is known, and begin() picks the
+  // lane of the actual nU.
+  struct Share {
+    int u, i_beg, n;
+  };
+  __device__ __forceinline__ static Share share(int nU, int I) {
+    const uint32_t G = gridDim.x, bx = blockIdx.x;
+    Share sh;
+    sh.u = (int)(bx * (uint32_t)nU / G);
+    const uint32_t lo = ((uint32_t)sh.u * G + nU - 1) / nU;         // first CTA of group u
+    const uint32_t hi = ((uint32_t)(sh.u + 1) * G + nU - 1) / nU;   // one past its last
+    const uint32_t c = hi - lo, r = bx - lo;
+    sh.i_beg = (int)((uint32_t)I * r / c);
+    sh.n = (int)((uint32_t)I * (r + 1) / c) - sh.i_beg;
+    return sh;
+  }
+
   __device__ __forceinline__ void set_stage() {
     valid = st < nst;
     if (!valid) return;
@@ -261,20 +283,17 @@ struct GuWalk {
     i0 = i_beg + st * kFusedNeurons;
     nn = n - st * kFusedNeurons < kFusedNeurons ? n - st * kFusedNeurons : kFusedNeurons;
   }
-  __device__ __forceinline__ void begin(int nU, const FusedParams& p) {
-    nkc = p.H / p.KC;
+  // Warp-collective: `mine` is this lane's share(lane + 1, I).
+  __device__ __forceinline__ void begin(int nU, const Share& mine, const FusedParams& p) {
+    nkc = p.nkc;
     kc = 0;
     st = 0;
     nst = 0;
     valid = false;
     if (nU <= 0) return;
-    const uint32_t G = gridDim.x, bx = blockIdx.x;
-    u = (int)(bx * (uint32_t)nU / G);
-    const uint32_t lo = ((uint32_t)u * G + nU - 1) / nU;         // first CTA of group u
-    const uint32_t hi = ((uint32_t)(u + 1) * G + nU - 1) / nU;   // one past its last
-    const uint32_t c = hi - lo, r = bx - lo;
-    i_beg = (int)((uint32_t)p.I * r / c);
-    n = (int)((uint32_t)p.I * (r + 1) / c) - i_beg;
+    u = __shfl_sync(kFull, mine.u, nU - 1);
+    i_beg = __shfl_sync(kFull, mine.i_beg, nU - 1);
+    n = __shfl_sync(kFull, mine.n, nU - 1);
     nst = (n + kFusedNeurons - 1) / kFusedNeurons;
     set_stage();
   }
@@ -294,10 +313,14 @@ struct DownWalk {
   int r0, r1, c0, rc, u0, ng, nU, RC, SR;
   bool valid;
 
-  __device__ __forceinline__ void begin(int nU_, const FusedParams& p) {
-    const uint32_t nrg = (uint32_t)(p.H / p.RG);
+  // The CTA's rows (grid values only, so known before the routing).
+  __device__ __forceinline__ void rows(const FusedParams& p) {
+    const uint32_t nrg = (uint32_t)p.nrg;
     r0 = (int)(nrg * blockIdx.x / gridDim.x) * p.RG;
     r1 = (int)(nrg * (blockIdx.x + 1) / gridDim.x) * p.RG;
+  }
+  // After rows().
+  __device__ __forceinline__ void begin(int nU_, const FusedParams& p) {
     nU = nU_;
     RC = p.RC;
     SR = p.SR;
@@ -386,7 +409,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   }
   __syncthreads();
   pdl_wait();      // x, topk_ids and topk_w come from upstream work
-  pdl_trigger();
+  // the routing first: every warp builds the expert schedule itself
+  WarpSchedule<KMAX> s;
+  s.load(p.ids, 1, p.k);
   if (warp == kFusedConsumers - 1 && lane == 0) {
     // this launch's index: launches are stream-ordered (and programmatic
     // dependents wait above for the previous one), so each adds gridDim.x
@@ -404,8 +429,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
       xf[b] = stage_block_f16(v, xs + 64 * b, b);
     }
   }
-  WarpSchedule<KMAX> s;
-  s.build(p.ids, 1, p.k, p.E, sm_words + warp * 32, p.err);
+  // the stage walks' grid arithmetic while the ids are in flight
+  const GuWalk::Share share = GuWalk::share(lane + 1, I);
+  DownWalk dw;
+  dw.rows(p);
+  s.finish(p.E, sm_words + warp * 32, p.err);
   const int nU = s.n_unique;
   const GuStageLayout lay(KC);
 
@@ -414,8 +442,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     // one ring for everything the CTA streams: its gate/up tiles, then its
     // down row groups, each into the next slot as soon as it is free
     GuWalk gw;
-    gw.begin(nU, p);
-    DownWalk dw;
+    gw.begin(nU, share, p);
     dw.begin(nU, p);
     RingPos rg(SG);
     int gi = 0;
@@ -434,7 +461,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
           // scales (full boxes; rows past the expert are never read)
           mbar_expect_tx(bar, 2u * kFusedNeurons * KC + 2u * kFusedNeurons * (KC >> 5));
           const int row = e * 2 * I + gw.i0;
-          const int kchunk = gw.kc * ((KC >> 2) / p.kin);
+          const int kchunk = gw.kc * p.kdiv;
           tma_load_3d(dst, &p.tm_codes, 0, kchunk, row, bar);
           tma_load_3d(dst + lay.up, &p.tm_codes, 0, kchunk, row + I, bar);
           tma_load_2d(dst + lay.gs, &p.tm_scales, gw.kc * (KC >> 7), row, bar);
@@ -458,6 +485,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
         dw.next();
       }
     }
+    // the next launch may start its setup (off this warp's critical path)
+    pdl_trigger();
     // never leave with copies in flight
     if (lane == 0) {
       RingPos r(SG);
@@ -469,6 +498,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
 
   // -------------------------------------------------------------- consumers
   named_sync(1, ncons);   // x staged
+  pdl_trigger();
 
   if (warp == 0) {
     // while the first tiles are in flight: per unique expert u (lane u), the
@@ -509,7 +539,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   RingPos rg(SG);
   {
     GuWalk gw;
-    gw.begin(nU, p);
+    gw.begin(nU, share, p);
     float ag = 0.f, au = 0.f;
     const int nbk = KC >> 5;                      // blocks per row per stage
     #pragma unroll 1
@@ -552,7 +582,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   // ---- down, one row chunk at a time: its groups sit in the ring slots
   // after the gate/up tiles; warp owns row c0 + warp and its lanes take the
   // chunk's items (expert u, block b), two at a time
-  DownWalk dw;
   dw.begin(nU, p);
   const int n_items = nU * nbI;
   int c0 = 0, rc = 0, ngr = 0;
