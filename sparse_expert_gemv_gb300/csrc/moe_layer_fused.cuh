@@ -108,13 +108,14 @@ struct FusedSmem {
   int ep;       // the value bar_ctr reaches when this launch's CTAs have all arrived
   int cf;       // [k] combined routing weight of each unique expert
   int jz;       // [k] first slot j routed to each unique expert
-  int bars;     // mbarriers: full[SG], empty[SG]
+  int bars;     // mbarriers: full[SG], empty[SG], then one for the h copy
   int words;    // 16 warps x 32 words of expert bitmap
   // h of each unique expert as f16 ([k][I/32] blocks of 64 bytes); then, per
   // down item t (block t % (I/32) of unique expert t / (I/32)), its FP32
   // factor (routing weight x block factor) and the shared-memory offsets of
   // its codes and scales in the current row chunk (row 0)
   int hs, tf, tc, ts;
+  int hraw;     // every unique expert's h row as read (bf16, [k][I])
   int total;
   __host__ __device__ FusedSmem(int SG, int slot_g, int H, int I, int k) {
     int o = SG * slot_g;
@@ -129,7 +130,7 @@ struct FusedSmem {
     jz = o;
     o += round128(k * 4);
     bars = o;
-    o += round128(2 * SG * 8);
+    o += round128((2 * SG + 1) * 8);
     words = o;
     o += 16 * 32 * 4;
     hs = o;
@@ -140,6 +141,8 @@ struct FusedSmem {
     o += round128(k * (I >> 5) * 4);
     ts = o;
     o += round128(k * (I >> 5) * 4);
+    hraw = o;
+    o += round128(k * I * 2);
     total = o;
   }
 };
@@ -390,6 +393,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   int* jz = reinterpret_cast<int*>(smem + L.jz);
   uint64_t* full_g = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty_g = full_g + SG;
+  uint64_t* full_h = empty_g + SG;     // the h rows' copy
   uint32_t* sm_words = reinterpret_cast<uint32_t*>(smem + L.words);
   const int ctid = threadIdx.x;                    // consumer thread index
   const int ncons = kFusedConsumers * 32;
@@ -405,6 +409,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
       mbar_init(&full_g[i], 1);
       mbar_init(&empty_g[i], kFusedConsumers);
     }
+    mbar_init(full_h, 1);
     mbar_init_fence();
   }
   __syncthreads();
@@ -622,15 +627,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     chunk_tables();
     chunk_wait();
   }
-  if (ctid == 0 && !grid_wait(p.bar_ctr, *bar_target, p.err)) dead = true;
-  named_sync(1, ncons);
-  // h of each unique expert -> f16 blocks (read through L2: other CTAs wrote
-  // it), and each block's factor times its expert's routing weight
+  if (ctid == 0) {
+    if (!grid_wait(p.bar_ctr, *bar_target, p.err)) dead = true;
+    // every unique expert's h row, one bulk copy each (the async proxy reads
+    // what other CTAs' generic stores wrote: fence between the proxies)
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    mbar_expect_tx(full_h, (uint32_t)(nU * I * 2));
+    for (int u = 0; u < nU; ++u)
+      bulk_copy_g2s(smem + L.hraw + (size_t)u * I * 2, p.h + (size_t)jz[u] * I, (uint32_t)(I * 2), full_h);
+  }
+  if (nU > 0 && !dead) dead = !mbar_wait(full_h, 0, p.err);
+  // h -> f16 blocks, and each block's factor times its expert's routing weight
   #pragma unroll 1
   for (int t = ctid; t < n_items; t += ncons) {
     const int u = t / nbI, b = t - u * nbI;
-    const uint4* src = reinterpret_cast<const uint4*>(p.h + (size_t)jz[u] * I) + 4 * b;
-    const uint4 v[4] = {__ldcg(src), __ldcg(src + 1), __ldcg(src + 2), __ldcg(src + 3)};
+    const uint4* src = reinterpret_cast<const uint4*>(smem + L.hraw + (size_t)u * I * 2) + 4 * b;
+    const uint4 v[4] = {src[0], src[1], src[2], src[3]};
     tf[t] = cf[u] * stage_block_f16(v, hs + 64 * t, b);
   }
   named_sync(1, ncons);   // h staged
