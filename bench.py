@@ -336,8 +336,10 @@ def run_ours(args, rank, world, local):
         launches = 2 * K
     traffic = recorded_traffic(kernel)
 
-    # end to end through the host-buffer entry point: pinned host inputs copied
-    # in, the layer, y copied out, every step
+    # end to end through the host-buffer entry point, every step: the step's
+    # pinned host inputs go to the device (read in place by the kernels
+    # through their device mapping), the layer runs, y comes back to pinned
+    # host memory, and the call waits for it
     xh = x_all.cpu().pin_memory()
     ih = ids_all.cpu().pin_memory()
     wh = w_all.cpu().pin_memory()

@@ -63,6 +63,8 @@ typedef enum {
 
 /* Flags of moe_decode_config_t. */
 #define MOE_FLAG_NO_PDL 0x1u       /* launch without programmatic dependent launch */
+#define MOE_FLAG_HOST_COPY 0x2u    /* moe_decode_forward_host always copies through
+                                      the device staging buffers */
 
 typedef struct {
   int32_t E;      /* experts, 1..1024 */
@@ -170,11 +172,16 @@ moe_status_t moe_decode_layer(moe_decode_t handle, int32_t T, const uint16_t* x,
                               uint16_t* h, uint16_t* y, void* stream);
 
 /*
- * The whole layer from and to HOST memory: copies x, topk_ids and topk_w to
- * the handle's device staging buffers, runs moe_decode_layer, copies y back
- * and waits for the stream. Host buffers should be pinned (cudaHostAlloc or
- * torch pin_memory) for asynchronous copies. T <= max_T. Calls on one handle
- * must not overlap (they share the staging buffers).
+ * The whole layer from and to HOST memory, waiting for the stream before it
+ * returns. The kernels read x, topk_ids and topk_w and write y in place when
+ * the device can address the host buffers: always on a device that accesses
+ * pageable host memory coherently (cudaDevAttrPageableMemoryAccess, e.g. a
+ * Grace-Blackwell part over its chip-to-chip link), else when all four are
+ * page-locked (cudaHostAlloc or torch pin_memory). Otherwise, or with
+ * MOE_FLAG_HOST_COPY, x, topk_ids and topk_w are copied to the handle's device
+ * staging buffers, moe_decode_layer runs, and y is copied back. h goes to the
+ * handle's staging buffer either way. T <= max_T. Calls on one handle must not
+ * overlap (they share the staging buffers).
  *   x_host [T,H] bf16, ids_host [T,k] int32, w_host [T,k] float, y_host [T,H] bf16 out
  */
 moe_status_t moe_decode_forward_host(moe_decode_t handle, int32_t T, const uint16_t* x_host,

@@ -10,9 +10,9 @@ decoded to FP32 in registers, one warp per output.
 The compute lives in libmoe_decode.so (C ABI, include/moe_decode.h). This
 package is a thin ctypes binding: PyTorch supplies device memory and streams.
 """
-from ._lib import (LIB_PATH, MOE_DEVICE_BAD_ID, MOE_DEVICE_TIMEOUT, MOE_FLAG_NO_PDL, MoEConfig,
-                   MoEError, check, lib)
+from ._lib import (LIB_PATH, MOE_DEVICE_BAD_ID, MOE_DEVICE_TIMEOUT, MOE_FLAG_HOST_COPY,
+                   MOE_FLAG_NO_PDL, MoEConfig, MoEError, check, lib)
 from .layer import MoEDecode
 
 __all__ = ["MoEDecode", "MoEError", "MoEConfig", "lib", "check", "LIB_PATH",
-           "MOE_DEVICE_BAD_ID", "MOE_DEVICE_TIMEOUT", "MOE_FLAG_NO_PDL"]
+           "MOE_DEVICE_BAD_ID", "MOE_DEVICE_TIMEOUT", "MOE_FLAG_HOST_COPY", "MOE_FLAG_NO_PDL"]

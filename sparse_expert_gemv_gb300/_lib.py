@@ -16,6 +16,7 @@ MOE_OK = 0
 MOE_DEVICE_BAD_ID = 0x1
 MOE_DEVICE_TIMEOUT = 0x2
 MOE_FLAG_NO_PDL = 0x1
+MOE_FLAG_HOST_COPY = 0x2
 MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 STATUS_NAMES = {

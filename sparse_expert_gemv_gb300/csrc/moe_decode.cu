@@ -38,6 +38,7 @@ struct moe_decode {
   size_t down_smem;
   size_t smem_per_block;          // opt-in shared-memory maximum of one CTA
   bool fused_ok;                  // the single-token fused kernel can run here
+  bool host_direct;               // the device reads pageable host memory coherently
   CUtensorMap tm_codes;           // W_gateup codes / scales and W_down codes / scales
   CUtensorMap tm_scales;          // as tensors for its TMA copies
   CUtensorMap tm_dcodes;
@@ -56,6 +57,17 @@ struct moe_decode {
 namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The device address of a page-locked host buffer mapped into the device's
+// address space, or null (pageable memory, or a device pointer).
+const void* mapped_host(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
 
 template <typename Kernel, typename... Args>
 cudaError_t launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
@@ -401,7 +413,7 @@ moe_status_t moe_decode_create(const moe_decode_config_t* cfg, const uint8_t* w_
   if (c.E < 1 || c.k < 1 || c.H < 1 || c.I < 1 || c.max_T < 0) return MOE_ERR_INVALID_ARG;
   if (c.k > c.E) return MOE_ERR_INVALID_ARG;
   if (c.E > kMaxE || c.k > kMaxK || c.H % 32 || c.I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if ((c.flags & ~MOE_FLAG_NO_PDL) != 0) return MOE_ERR_INVALID_ARG;
+  if ((c.flags & ~(MOE_FLAG_NO_PDL | MOE_FLAG_HOST_COPY)) != 0) return MOE_ERR_INVALID_ARG;
   const size_t down_smem = (size_t)c.k * c.I * sizeof(float);
   if (down_smem > kMaxDownSmem) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(w_gateup, 32) || !aligned(w_down, 32)) return MOE_ERR_MISALIGNED;
@@ -419,6 +431,10 @@ moe_status_t moe_decode_create(const moe_decode_config_t* cfg, const uint8_t* w_
                 cudaSuccess &&
             cudaMalloc(&m->d_err, 32) == cudaSuccess && cudaMemset(m->d_err, 0, 32) == cudaSuccess;
   if (ok) m->d_bar = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(m->d_err) + 8);
+  int pageable = 0;
+  ok = ok && cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, m->device) ==
+                 cudaSuccess;
+  m->host_direct = pageable != 0;
   ok = ok && query_fused(m);
 
 
@@ -545,6 +561,21 @@ moe_status_t moe_decode_forward_host(moe_decode_t m, int32_t T, const uint16_t* 
   if (!x_host || !ids_host || !w_host || !y_host) return MOE_ERR_INVALID_ARG;
   const moe_decode_config_t& c = m->cfg;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // host buffers the device can address are read and written by the kernels
+  // in place, with no copy-engine round trips: any host memory on a device
+  // that accesses pageable memory coherently (at the host's addresses), else
+  // page-locked buffers through their device mapping
+  const bool copy = (c.flags & MOE_FLAG_HOST_COPY) != 0;
+  const void* xd = copy ? nullptr : m->host_direct ? x_host : mapped_host(x_host);
+  const void* idd = copy ? nullptr : m->host_direct ? ids_host : mapped_host(ids_host);
+  const void* wd = copy ? nullptr : m->host_direct ? w_host : mapped_host(w_host);
+  void* yd = copy ? nullptr : m->host_direct ? y_host : const_cast<void*>(mapped_host(y_host));
+  if (xd && idd && wd && yd) {
+    st = moe_decode_layer(m, T, static_cast<const uint16_t*>(xd), static_cast<const int32_t*>(idd),
+                          static_cast<const float*>(wd), m->d_h, static_cast<uint16_t*>(yd), stream);
+    if (st != MOE_OK) return st;
+    return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   if (cudaMemcpyAsync(m->d_x, x_host, (size_t)T * c.H * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(m->d_ids, ids_host, (size_t)T * c.k * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(m->d_w, w_host, (size_t)T * c.k * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
@@ -673,7 +704,7 @@ extern "C" moe_status_t moe_decode_layer_noalloc(const moe_decode_config_t* cfg,
   if (c.E < 1 || c.k < 1 || c.H < 1 || c.I < 1 || T < 0) return MOE_ERR_INVALID_ARG;
   if (c.k > c.E) return MOE_ERR_INVALID_ARG;
   if (c.E > kMaxE || c.k > kMaxK || c.H % 32 || c.I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if ((c.flags & ~MOE_FLAG_NO_PDL) != 0) return MOE_ERR_INVALID_ARG;
+  if ((c.flags & ~(MOE_FLAG_NO_PDL | MOE_FLAG_HOST_COPY)) != 0) return MOE_ERR_INVALID_ARG;
   if ((size_t)c.k * c.I * sizeof(float) > kMaxDownSmem) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((size_t)T * c.k * c.I * 2 > kNoAllocHBytes) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(w_gateup, 32) || !aligned(w_down, 32)) return MOE_ERR_MISALIGNED;

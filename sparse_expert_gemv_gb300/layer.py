@@ -12,16 +12,29 @@ import torch
 from ._lib import MoEConfig, check, lib
 
 
-def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
-    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+def _ptr(t: torch.Tensor | None) -> int:
+    # a plain int: the entry points' argtypes make it a void*
+    return 0 if t is None else t.data_ptr()
 
 
-def _stream(stream: torch.cuda.Stream | None) -> ctypes.c_void_p:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+def _stream(stream: torch.cuda.Stream | None) -> int:
+    if stream is not None:
+        return stream.cuda_stream
+    # the current stream's handle, without building a Stream object per call
+    # where torch offers that
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
+
+
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _need(t: torch.Tensor, dtype: torch.dtype, shape: tuple, name: str, cuda: bool = True) -> None:
+    # one cheap test on the common path; the detailed ones only on failure
+    if (isinstance(t, torch.Tensor) and t.dtype is dtype and t.shape == shape
+            and t.is_cuda is cuda and t.is_contiguous()):
+        return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
@@ -32,8 +45,7 @@ def _need(t: torch.Tensor, dtype: torch.dtype, shape: tuple, name: str, cuda: bo
         raise ValueError(f"{name} must be contiguous")
     if cuda and not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if not cuda and t.is_cuda:
-        raise ValueError(f"{name} must be a host tensor")
+    raise ValueError(f"{name} must be a host tensor")
 
 
 class MoEDecode:

@@ -179,17 +179,30 @@ def test_bitwise_deterministic_and_graph_capture(dev):
 
 
 def test_no_pdl_flag_and_host_path(dev):
-    from sparse_expert_gemv_gb300 import MOE_FLAG_NO_PDL
+    from sparse_expert_gemv_gb300 import MOE_FLAG_HOST_COPY, MOE_FLAG_NO_PDL
     a = Small(dev, 8, 4, 512, 128, 6)
     b = Small(dev, 8, 4, 512, 128, 6, flags=MOE_FLAG_NO_PDL)
+    c = Small(dev, 8, 4, 512, 128, 6, flags=MOE_FLAG_HOST_COPY)
     _, ya = a.run()
     _, yb = b.run()
     assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
+    want = ya.cpu().view(torch.int16)
     x = torch.from_numpy(a.x_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
     ids = torch.from_numpy(a.ids).pin_memory()
     tw = torch.from_numpy(a.tw).pin_memory()
+    # pinned host buffers, read and written in place by the kernels
     yh = a.layer.forward_host(x, ids, tw)
-    assert torch.equal(yh.view(torch.int16), ya.cpu().view(torch.int16))
+    assert torch.equal(yh.view(torch.int16), want)
+    # pageable host buffers: in place where the device reaches pageable
+    # memory, else through the staging copies; same result
+    yp = torch.empty_like(yh, pin_memory=False)
+    a.layer.forward_host(x.clone(), ids.clone(), tw.clone(), y=yp)
+    assert not yp.is_pinned()
+    assert torch.equal(yp.view(torch.int16), want)
+    # the staging copies, forced
+    for xx, ii, ww in ((x, ids, tw), (x.clone(), ids.clone(), tw.clone())):
+        yc = c.layer.forward_host(xx, ii, ww)
+        assert torch.equal(yc.view(torch.int16), want)
 
 
 def test_bad_arguments_raise(dev):
