@@ -16,6 +16,10 @@ exchange step on one GPU); value = all ranks' tokens / the slowest rank's time.
 
 --impl reference times the CPU oracle (float64 numpy) on the host cores on a
 bounded sample of the same workload.
+
+--workload N runs one of the other configurations instead (0: tiny, 2: T=8,
+3: Zipf-skewed T=32, 4: large experts T=16), for reports; the default line is
+workload 1.
 """
 from __future__ import annotations
 
@@ -55,6 +59,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--cpu-sample-s", type=float, default=12.0)
+    # the other configurations, for reports (the default line is workload 1)
+    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=sorted(wl.WORKLOADS))
     return ap.parse_args()
 
 
@@ -191,8 +197,8 @@ def cpu_oracle_rate(w, seed, experts, budget_s):
 
 
 def run_reference(args, rank, world):
-    w = wl.workload(WORKLOAD)
-    seed = wl.seed_of(WORKLOAD)
+    w = wl.workload(args.workload)
+    seed = wl.seed_of(args.workload)
     if rank != 0:
         return
     # the oracle needs only the routed experts; generate them lazily
@@ -229,15 +235,33 @@ def run_ours(args, rank, world, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = wl.workload(WORKLOAD)
-    seed = wl.seed_of(WORKLOAD)
+    w = wl.workload(args.workload)
+    seed = wl.seed_of(args.workload)
     K, W, L = args.steps, args.warmup, args.layers
     T, E, k, H, I = w.T, w.E, w.k, w.H, w.I
 
-    # one layer's MXFP8 weights, L resident copies at distinct addresses
-    experts = wl.make_experts(w, seed, range(E))
-    host = [np.stack([experts[e][i] for e in range(E)]) for i in range(4)]
-    base = [torch.from_numpy(a).to(dev) for a in host]
+    # one layer's MXFP8 weights, L resident copies at distinct addresses; a
+    # layer of several GB (workload 4) gets random MXFP8 bytes generated on the
+    # device instead (the timing does not depend on the values; no oracle leg)
+    big = w.E * w.weight_bytes_per_expert > 4e9
+    if big:
+        L = min(L, 2)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+
+        def codes(*shape):
+            c = torch.randint(0, 0xFE, shape, dtype=torch.uint8, device=dev, generator=gen)
+            return c.masked_fill_(c == 0x7F, 0x7E)            # no NaN codes
+
+        def scales(*shape):
+            return torch.randint(118, 124, shape, dtype=torch.uint8, device=dev, generator=gen)
+
+        experts = None
+        base = [codes(E, 2 * I, H), scales(E, 2 * I, H // 32), codes(E, H, I), scales(E, H, I // 32)]
+    else:
+        experts = wl.make_experts(w, seed, range(E))
+        host = [np.stack([experts[e][i] for e in range(E)]) for i in range(4)]
+        base = [torch.from_numpy(a).to(dev) for a in host]
     layers = []
     for _ in range(L):
         t = [b.clone() for b in base]
@@ -360,7 +384,7 @@ def run_ours(args, rank, world, local):
     ref_ok = torch.equal(yh.view(torch.int16), y[W + K - 1].cpu().view(torch.int16))
 
     cpu = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and experts is not None:
         r, n, cdt = cpu_oracle_rate(w, seed, experts, args.cpu_sample_s)
         cpu = {"value": r, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} decode steps of the workload (T={T}, fresh routing each), "
@@ -375,7 +399,8 @@ def run_ours(args, rank, world, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {
                 "workload": w.name, "E": E, "k": k, "H": H, "I": I, "T": T,
-                "weights": "MXFP8 (E4M3 + UE8M0 per 32), bf16 activations, FP32 accumulate",
+                "weights": "MXFP8 (E4M3 + UE8M0 per 32), bf16 activations, FP32 accumulate"
+                           + (" (random bytes generated on the device: timing only)" if big else ""),
                 "layers_rotated": L,
                 "l2": f"inputs larger than L2: {L} resident layer copies "
                       f"({L * w.E * w.weight_bytes_per_expert / 1e9:.1f} GB) with fresh routing "
