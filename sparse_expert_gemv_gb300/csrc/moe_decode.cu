@@ -91,6 +91,16 @@ bool use_pdl(const moe_decode* m) { return (m->cfg.flags & MOE_FLAG_NO_PDL) == 0
 
 template <int NT, int KMAX>
 cudaError_t launch_gate_up_t(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
+  // several tokens whose x fits in shared memory: staged once per CTA as f16
+  // blocks (one 16-warp CTA per SM)
+  const size_t xs = moe::gate_up_xs_smem(p.T, p.H);
+  if (p.T >= 2 && xs <= m->smem_per_block) {
+    const long long units_max = (long long)std::min(p.E, p.T * p.k) * p.I;
+    const long long ctas_needed = (units_max + moe::kXsWarps - 1) / moe::kXsWarps;
+    const int grid = (int)std::max(1LL, std::min(ctas_needed, (long long)m->num_sms));
+    return launch(moe::moe_gate_up_xs<NT, KMAX>, dim3(grid), dim3(moe::kXsThreads), xs, s,
+                  use_pdl(m), p);
+  }
   const long long units_max = (long long)std::min(p.E, p.T * p.k) * p.I;
   const long long ctas_needed = (units_max + moe::kWarps - 1) / moe::kWarps;
   const long long cap = (long long)m->num_sms * m->gate_up_ctas_per_sm;
@@ -284,6 +294,19 @@ cudaError_t launch_fused(const moe_decode* m, const moe::FusedParams& fp, size_t
 // Device limits shared by handles and the allocation-free call: SM count,
 // gate/up occupancy, shared memory, and whether the fused kernel fits one CTA
 // per SM (it then runs as a cooperative launch of num_sms CTAs).
+// The shared-memory limit of the gate/up kernels that stage x: the device's
+// opt-in maximum.
+cudaError_t set_xs_attributes(size_t smem) {
+  cudaError_t e = cudaSuccess;
+  for (const void* f : {(const void*)moe::moe_gate_up_xs<1, 8>, (const void*)moe::moe_gate_up_xs<2, 8>,
+                        (const void*)moe::moe_gate_up_xs<4, 8>, (const void*)moe::moe_gate_up_xs<8, 8>,
+                        (const void*)moe::moe_gate_up_xs<1, 32>, (const void*)moe::moe_gate_up_xs<2, 32>,
+                        (const void*)moe::moe_gate_up_xs<4, 32>, (const void*)moe::moe_gate_up_xs<8, 32>})
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return e;
+}
+
 bool query_fused(moe_decode* m) {
   int v_blk = 0, coop = 0;
   if (cudaDeviceGetAttribute(&v_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device) !=
@@ -291,6 +314,7 @@ bool query_fused(moe_decode* m) {
       cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, m->device) != cudaSuccess)
     return false;
   m->smem_per_block = (size_t)v_blk;
+  if (set_xs_attributes(m->smem_per_block) != cudaSuccess) return false;
   m->fused_ok = false;
   if (!coop || set_fused_attributes(m->smem_per_block) != cudaSuccess) return true;
   moe::FusedParams fp = {};
