@@ -98,7 +98,7 @@ cudaError_t launch_gate_up_t(const moe_decode* m, const moe::GateUpParams& p, cu
     const long long units_max = (long long)std::min(p.E, p.T * p.k) * p.I;
     const long long ctas_needed = (units_max + moe::kXsWarps - 1) / moe::kXsWarps;
     const int grid = (int)std::max(1LL, std::min(ctas_needed, (long long)m->num_sms));
-    return launch(moe::moe_gate_up_xs<NT, KMAX>, dim3(grid), dim3(moe::kXsThreads), xs, s,
+    return launch(moe::moe_gate_up_3d_batched_xs<NT, KMAX>, dim3(grid), dim3(moe::kXsThreads), xs, s,
                   use_pdl(m), p);
   }
   const long long units_max = (long long)std::min(p.E, p.T * p.k) * p.I;
@@ -127,8 +127,8 @@ cudaError_t launch_gate_up(const moe_decode* m, const moe::GateUpParams& p, cuda
 constexpr int kDownQ = 8;
 
 cudaError_t launch_down(const moe_decode* m, const moe::DownParams& p, cudaStream_t s) {
-  return launch(moe::moe_down_3d_batched<kDownQ>, dim3(p.H / moe::kWarps, p.T),
-                dim3(moe::kThreads), m->down_smem, s, use_pdl(m), p);
+  return launch(moe::moe_down_3d_batched<kDownQ>, dim3(p.H / moe::kWarps, p.T), dim3(moe::kThreads),
+                moe::down_xs_smem(p.k, p.I), s, use_pdl(m), p);
 }
 
 // ---- single-token fused layer ----------------------------------------------
@@ -298,10 +298,10 @@ cudaError_t launch_fused(const moe_decode* m, const moe::FusedParams& fp, size_t
 // opt-in maximum.
 cudaError_t set_xs_attributes(size_t smem) {
   cudaError_t e = cudaSuccess;
-  for (const void* f : {(const void*)moe::moe_gate_up_xs<1, 8>, (const void*)moe::moe_gate_up_xs<2, 8>,
-                        (const void*)moe::moe_gate_up_xs<4, 8>, (const void*)moe::moe_gate_up_xs<8, 8>,
-                        (const void*)moe::moe_gate_up_xs<1, 32>, (const void*)moe::moe_gate_up_xs<2, 32>,
-                        (const void*)moe::moe_gate_up_xs<4, 32>, (const void*)moe::moe_gate_up_xs<8, 32>})
+  for (const void* f : {(const void*)moe::moe_gate_up_3d_batched_xs<1, 8>, (const void*)moe::moe_gate_up_3d_batched_xs<2, 8>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<4, 8>, (const void*)moe::moe_gate_up_3d_batched_xs<8, 8>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<1, 32>, (const void*)moe::moe_gate_up_3d_batched_xs<2, 32>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<4, 32>, (const void*)moe::moe_gate_up_3d_batched_xs<8, 32>})
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   return e;

@@ -7,7 +7,7 @@
 // shfl.xor butterfly. No warp shares partial sums with another.
 #pragma once
 
-#include "moe_device.cuh"
+#include "moe_f16blocks.cuh"
 
 namespace moe {
 
@@ -275,12 +275,11 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gate_up_3d_batched(GateUpPara
 // One warp per (token t, output row r); a CTA covers 8 consecutive rows of one
 // token. The warp's k rows Wd[e_j, r, :] are laid out as k*I/32 blocks of 32
 // elements and dealt to the lanes (block f = j*I/32 + b to lane f % 32), so all
-// 32 lanes stream even when I/32 < 32. h[t] (k*I bf16) is read once per CTA
-// into shared memory as FP32, 16-byte chunks XOR-swizzled by block index so
-// that lanes reading consecutive blocks hit distinct banks. The routing weight
-// multiplies each block's scaled partial inside the single FP32 accumulator.
-// With `early` set, the first round of weight loads is issued before waiting
-// for the gate/up kernel (those rows depend only on topk_ids).
+// 32 lanes stream even when I/32 < 32; down_load_round fetches one round of
+// them. The kernel (moe_down_3d_batched, below) reads h[t] once per CTA into
+// shared memory as f16 blocks. With `early` set, the
+// first round of weight loads is issued before waiting for the gate/up kernel
+// (those rows depend only on topk_ids).
 // ---------------------------------------------------------------------------
 
 struct DownParams {
@@ -321,37 +320,164 @@ __device__ __forceinline__ void down_load_round(const DownParams& p, int f0, int
   }
 }
 
+// ---------------------------------------------------------------------------
+// Gate/up for several tokens with x staged in shared memory (T >= 2 when the
+// T tokens' x fits): the work units and token groups of
+// moe_gate_up_3d_batched, but each CTA converts x once to f16 blocks scaled
+// by a power of two (as the one-launch kernel does), each weight block is
+// decoded once to f16 pairs for all of a group's tokens, and fma.rn.f32.f16
+// forms every product (exact, as the header explains).
+// ---------------------------------------------------------------------------
+
+constexpr int kXsWarps = 16;
+constexpr int kXsThreads = kXsWarps * 32;
+
+// Shared-memory bytes of moe_gate_up_3d_batched_xs for T tokens of H (all of it dynamic:
+// the warps' schedule words, then x as f16 blocks, then their factors).
+__host__ __device__ constexpr size_t gate_up_xs_smem(int T, int H) {
+  return (size_t)kXsWarps * 32 * 4 + (size_t)T * (H >> 5) * (64 + 4);
+}
+
+template <int NT, int KMAX>
+__global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_3d_batched_xs(GateUpParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  const int H = p.H, I = p.I, nb = H >> 5;
+  uint32_t* sm_words = reinterpret_cast<uint32_t*>(smem);              // [warps][32]
+  uint8_t* xs = smem + kXsWarps * 32 * 4;                              // [T][nb] x blocks
+  float* xf = reinterpret_cast<float*>(xs + (size_t)p.T * nb * 64);    // [T][nb] factors
+  pdl_wait();      // x and topk_ids come from upstream work
+  pdl_trigger();   // the down kernel may start fetching its weights
+  WarpSchedule<KMAX> s;
+  s.load(p.ids, p.T, p.k);
+  // x -> f16 blocks while the ids are in flight
+#pragma unroll 1
+  for (int idx = threadIdx.x; idx < p.T * nb; idx += kXsThreads) {
+    const int t = idx / nb, b = idx - t * nb;
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H) + 4 * b;
+    const uint4 v[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3)};
+    xf[idx] = stage_block_f16(v, xs + 64 * idx, b);
+  }
+  s.finish(p.E, sm_words + wid * 32, p.err);
+  // A slot with an out-of-range id gets no unit; its h slice is defined as zero.
+  if (__any_sync(kFull, s.badmask != 0u)) {
+    for (int t = blockIdx.x * kXsWarps + wid; t < p.T; t += gridDim.x * kXsWarps) {
+      const uint32_t bm = __shfl_sync(kFull, s.badmask, t);
+      for (uint32_t m = bm; m; m &= m - 1) {
+        uint16_t* row = p.h + ((size_t)t * p.k + (__ffs(m) - 1)) * I;
+        for (int i = lane; i < I; i += 32) row[i] = 0;
+      }
+    }
+  }
+  __syncthreads();   // x staged
+  const LaneBlock lb(lane);
+  const bool swap = lb.c_first != 0;
+  const long long units = (long long)s.n_unique * I;
+#pragma unroll 1
+  for (long long unit = (long long)blockIdx.x * kXsWarps + wid; unit < units;
+       unit += (long long)gridDim.x * kXsWarps) {
+    const int u = (int)(unit / I);
+    const int i = (int)(unit - (long long)u * I);
+    const int e = s.expert(u);
+    const uint32_t jm = s.jmask(e);
+    uint32_t tokens = __ballot_sync(kFull, jm != 0u);
+    const size_t row = (size_t)e * 2 * I + i;
+    const uint8_t* wg = p.wgu + row * H;
+    const uint8_t* wu = wg + (size_t)I * H;
+    const uint8_t* sg = p.sgu + row * nb;
+    const uint8_t* su = sg + (size_t)I * nb;
+#pragma unroll 1
+    while (tokens) {
+      int tok[NT];
+      int nt = 0;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        tok[n] = tokens ? __ffs(tokens) - 1 : 0;
+        if (tokens) {
+          tokens &= tokens - 1;
+          ++nt;
+        }
+      }
+      float ag[NT], au[NT];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
+      // the next block's codes are in flight while this one is applied
+      uint32_t qg[8], qu[8];
+      uint32_t s_g = 0, s_u = 0;
+      int b = lane;
+      if (b < nb) {
+        ld_weights32(wg + b * 32, qg);
+        ld_weights32(wu + b * 32, qu);
+        s_g = ld_scale(sg + b);
+        s_u = ld_scale(su + b);
+      }
+#pragma unroll 1
+      for (; b < nb; b += 32) {
+        uint32_t whg[16], whu[16];
+        decode_block_f16(qg, swap, whg);
+        decode_block_f16(qu, swap, whu);
+        const float scg = ue8m0_to_f32(s_g), scu = ue8m0_to_f32(s_u);
+        if (b + 32 < nb) {
+          ld_weights32(wg + (b + 32) * 32, qg);
+          ld_weights32(wu + (b + 32) * 32, qu);
+          s_g = ld_scale(sg + b + 32);
+          s_u = ld_scale(su + b + 32);
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          if (n < nt) {
+            const int xb = tok[n] * nb + b;
+            const uint8_t* act = xs + 64 * xb;
+            const float fx = xf[xb];
+            ag[n] = fmaf(dot_block_h(whg, act, lb) * fx, scg, ag[n]);
+            au[n] = fmaf(dot_block_h(whu, act, lb) * fx, scu, au[n]);
+          }
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        if (n < nt) {
+          const float g = warp_sum(ag[n]);
+          const float up = warp_sum(au[n]);
+          const uint32_t jt = __shfl_sync(kFull, jm, tok[n]);
+          const uint16_t hb = f32_to_bf16_rn((g / (1.0f + expf(-g))) * up);
+          if (lane < p.k && ((jt >> lane) & 1u)) p.h[((size_t)tok[n] * p.k + lane) * I + i] = hb;
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The down kernel: the work layout above (one warp per (token t, output row
+// r), the k rows' 32-element blocks dealt to the lanes, a CTA covering 8 rows
+// of one token); h[t] is converted once per CTA to power-of-two-scaled f16
+// blocks, keyed by the flat block index f = j * I/32 + b so that lane f % 32
+// reads its own swizzle, and each weight block is decoded to f16 pairs for
+// fma.rn.f32.f16.
+// ---------------------------------------------------------------------------
+
+__host__ __device__ constexpr size_t down_xs_smem(int k, int I) {
+  return (size_t)k * (I >> 5) * (64 + 4);
+}
+
 template <int QMAX>
-__device__ __forceinline__ float down_compute_round(const float4* __restrict__ sh, int f0,
-                                                    const uint32_t (&q)[QMAX][8],
-                                                    const float (&sc)[QMAX],
-                                                    const float (&wsel)[QMAX],
-                                                    const bool (&valid)[QMAX], float acc) {
+__device__ __forceinline__ float down_compute_round_xs(const uint8_t* hs, const float* hfac, int f0,
+                                                       const uint32_t (&q)[QMAX][8],
+                                                       const float (&sc)[QMAX],
+                                                       const float (&wsel)[QMAX],
+                                                       const bool (&valid)[QMAX],
+                                                       const LaneBlock& lb, bool swap, float acc) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int qi = 0; qi < QMAX; ++qi) {
     if (valid[qi]) {
-      const int blk = f0 + lane + 32 * qi;
-      const float4* hb = sh + (size_t)blk * 8;
-      const int sw = blk & 7;
-      float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float wv[8];
-        e4m3x4_to_f32(q[qi][2 * c], wv[0], wv[1], wv[2], wv[3]);
-        e4m3x4_to_f32(q[qi][2 * c + 1], wv[4], wv[5], wv[6], wv[7]);
-        const float4 h0 = hb[(2 * c) ^ sw];
-        const float4 h1 = hb[(2 * c + 1) ^ sw];
-        a0 = fmaf(wv[0], h0.x, a0);
-        a1 = fmaf(wv[1], h0.y, a1);
-        a0 = fmaf(wv[2], h0.z, a0);
-        a1 = fmaf(wv[3], h0.w, a1);
-        a0 = fmaf(wv[4], h1.x, a0);
-        a1 = fmaf(wv[5], h1.y, a1);
-        a0 = fmaf(wv[6], h1.z, a0);
-        a1 = fmaf(wv[7], h1.w, a1);
-      }
-      acc = fmaf((a0 + a1) * sc[qi], wsel[qi], acc);
+      const int f = f0 + lane + 32 * qi;
+      uint32_t wh[16];
+      decode_block_f16(q[qi], swap, wh);
+      const float d = dot_block_h(wh, hs + 64 * f, lb);
+      acc = fmaf(d * hfac[f] * sc[qi], wsel[qi], acc);
     }
   }
   return acc;
@@ -359,12 +485,14 @@ __device__ __forceinline__ float down_compute_round(const float4* __restrict__ s
 
 template <int QMAX>
 __global__ void __launch_bounds__(kThreads, 2) moe_down_3d_batched(DownParams p) {
-  extern __shared__ float4 sh_h[];   // [k*I/32 blocks][8 chunks] FP32, swizzled
+  extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   const int t = blockIdx.y;
   const int r = blockIdx.x * kWarps + wid;
   const int k = p.k, I = p.I, nbI = I >> 5, nf = k * nbI;
+  uint8_t* hs = smem;                                            // [nf] blocks of 64 B
+  float* hfac = reinterpret_cast<float*>(smem + (size_t)nf * 64);  // [nf] factors
   if (!p.early) pdl_wait();
   int id = -1;
   float wj = 0.f;
@@ -382,24 +510,22 @@ __global__ void __launch_bounds__(kThreads, 2) moe_down_3d_batched(DownParams p)
   down_load_round<QMAX>(p, 0, nf, nbI, r, id, wj, q, sc, wsel, valid);
   if (p.early) pdl_wait();   // h is written by the gate/up kernel
   {
-    const uint16_t* ht = p.h + (size_t)t * k * I;
-    const int nchunk = (k * I) >> 3;   // 8 bf16 per 16-byte load
-    for (int c = threadIdx.x; c < nchunk; c += kThreads) {
-      const uint4 v = *reinterpret_cast<const uint4*>(ht + (size_t)c * 8);
-      const int blk = c >> 2;
-      const int ch = (2 * c) & 7;
-      const int sw = blk & 7;
-      sh_h[blk * 8 + (ch ^ sw)] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
-      sh_h[blk * 8 + ((ch + 1) ^ sw)] =
-          make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+    const uint4* ht = reinterpret_cast<const uint4*>(p.h + (size_t)t * k * I);
+#pragma unroll 1
+    for (int f = threadIdx.x; f < nf; f += kThreads) {
+      const uint4* src = ht + 4 * f;
+      const uint4 v[4] = {src[0], src[1], src[2], src[3]};
+      hfac[f] = stage_block_f16(v, hs + 64 * f, f);
     }
   }
   __syncthreads();
   pdl_trigger();
-  float acc = down_compute_round<QMAX>(sh_h, 0, q, sc, wsel, valid, 0.f);
+  const LaneBlock lb(lane);
+  const bool swap = lb.c_first != 0;
+  float acc = down_compute_round_xs<QMAX>(hs, hfac, 0, q, sc, wsel, valid, lb, swap, 0.f);
   for (int f0 = 32 * QMAX; f0 < nf; f0 += 32 * QMAX) {
     down_load_round<QMAX>(p, f0, nf, nbI, r, id, wj, q, sc, wsel, valid);
-    acc = down_compute_round<QMAX>(sh_h, f0, q, sc, wsel, valid, acc);
+    acc = down_compute_round_xs<QMAX>(hs, hfac, f0, q, sc, wsel, valid, lb, swap, acc);
   }
   acc = warp_sum(acc);
   if (lane == 0) p.y[(size_t)t * p.H + r] = f32_to_bf16_rn(acc);

@@ -147,107 +147,6 @@ struct FusedSmem {
   }
 };
 
-// Byte offset, inside a 64-byte block of 32 f16 values, of its 16-byte chunk c
-// (values 8c .. 8c+7). Eight lanes reading eight consecutive blocks (a quarter
-// warp, one shared-memory wavefront of 16-byte loads) ask for chunk 2f + i
-// (i fixed, f = bit 2 of the block) in lanes with f = 0 and chunk 2(1 - f) + i
-// in the others; XOR-ing the chunk index with bit 1 of the block then puts the
-// eight loads in eight distinct 16-byte bank groups.
-__device__ __forceinline__ int chunk_off(int block, int c) { return 16 * (c ^ ((block >> 1) & 1)); }
-
-// 2^n as FP32 for -127 <= n <= 127, built from its bit pattern.
-__device__ __forceinline__ float exp2i(int n) {
-  return __uint_as_float(n > -127 ? (uint32_t)(n + 127) << 23 : 0x00400000u);
-}
-
-// One 32-element block of bf16 values (four uint4) -> f16 scaled by 2^e with
-// the block's largest magnitude in [2^14, 2^15), written to a 64-byte block
-// of shared memory; returns the factor 2^-e. A block of zeros (or of bf16
-// subnormals only) takes e = 127; Inf and NaN stay Inf and NaN.
-__device__ __forceinline__ float stage_block_f16(const uint4 (&v)[4], uint8_t* dst, int block) {
-  uint32_t m = 0;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint32_t ww[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) m = max(m, max(ww[i] & 0x7fffu, (ww[i] >> 16) & 0x7fffu));
-  }
-  const int e = min(141 - (int)(m >> 7), 127);   // 14 - (biased exponent - 127)
-  const float up = exp2i(e);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint32_t ww[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half2 hh = __floats2half2_rn(bf16_lo(ww[i]) * up, bf16_hi(ww[i]) * up);
-      o[i] = *reinterpret_cast<const uint32_t*>(&hh);
-    }
-    *reinterpret_cast<uint4*>(dst + chunk_off(block, c)) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  return exp2i(-e);
-}
-
-// Four E4M3 codes (one word, byte n = element n) times four f16 activations
-// (two f16x2 words), added to two FP32 accumulators.
-__device__ __forceinline__ void fma_e4m3x4(float& p, float& q, uint32_t codes, uint32_t x01,
-                                           uint32_t x23) {
-  asm("{\n\t.reg .b16 c0, c1;\n\t.reg .b32 lo, hi;\n\t"
-      ".reg .f16 w0, w1, w2, w3, v0, v1, v2, v3;\n\t"
-      "mov.b32 {c0, c1}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 lo, c0;\n\tcvt.rn.f16x2.e4m3x2 hi, c1;\n\t"
-      "mov.b32 {w0, w1}, lo;\n\tmov.b32 {w2, w3}, hi;\n\t"
-      "mov.b32 {v0, v1}, %3;\n\tmov.b32 {v2, v3}, %4;\n\t"
-      "fma.rn.f32.f16 %0, w0, v0, %0;\n\tfma.rn.f32.f16 %1, w1, v1, %1;\n\t"
-      "fma.rn.f32.f16 %0, w2, v2, %0;\n\tfma.rn.f32.f16 %1, w3, v3, %1;\n\t}"
-      : "+f"(p), "+f"(q)
-      : "r"(codes), "r"(x01), "r"(x23));
-}
-
-// 16 codes (one uint4) against 16 f16 activations (two uint4).
-__device__ __forceinline__ void fma_e4m3x16(float& p, float& q, const uint4 c, const uint4 x0,
-                                            const uint4 x1) {
-  fma_e4m3x4(p, q, c.x, x0.x, x0.y);
-  fma_e4m3x4(p, q, c.y, x0.z, x0.w);
-  fma_e4m3x4(p, q, c.z, x1.x, x1.y);
-  fma_e4m3x4(p, q, c.w, x1.z, x1.w);
-}
-
-// A lane's view of one 32-element block: which 16-code half it reads first
-// (alternating between groups of four lanes, so that a warp's 16-byte code
-// loads at a 32-byte lane stride are free of bank conflicts) and the byte
-// offsets of the matching activation chunks. Blocks a lane visits differ by
-// multiples of 8, so this depends on the lane alone.
-struct LaneBlock {
-  int c_first, c_second;   // code half offsets (0 or 16)
-  int x0, x1, x2, x3;      // activation chunk offsets for the first and second half
-  __device__ __forceinline__ explicit LaneBlock(int lane) {
-    const int f = (lane >> 2) & 1;
-    c_first = 16 * f;
-    c_second = 16 * (1 - f);
-    x0 = chunk_off(lane, 2 * f);
-    x1 = chunk_off(lane, 2 * f + 1);
-    x2 = chunk_off(lane, 2 * (1 - f));
-    x3 = chunk_off(lane, 2 * (1 - f) + 1);
-  }
-};
-
-// Dot product of one block: 32 codes at `codes` (shared memory) against the
-// f16 activation block at `act`.
-__device__ __forceinline__ float dot_block(const uint8_t* codes, const uint8_t* act,
-                                           const LaneBlock& lb) {
-  const uint4 a = *reinterpret_cast<const uint4*>(codes + lb.c_first);
-  const uint4 b = *reinterpret_cast<const uint4*>(codes + lb.c_second);
-  const uint4 x0 = *reinterpret_cast<const uint4*>(act + lb.x0);
-  const uint4 x1 = *reinterpret_cast<const uint4*>(act + lb.x1);
-  const uint4 x2 = *reinterpret_cast<const uint4*>(act + lb.x2);
-  const uint4 x3 = *reinterpret_cast<const uint4*>(act + lb.x3);
-  float p = 0.f, q = 0.f, r = 0.f, s = 0.f;
-  fma_e4m3x16(p, q, a, x0, x1);
-  fma_e4m3x16(r, s, b, x2, x3);
-  return (p + q) + (r + s);
-}
-
 // The CTA's gate/up stage sequence. The grid is split into one group of
 // CTAs per unique expert (gridDim.x >= nU; group sizes differ by at most one)
 // and each CTA of a group takes an equal share of that expert's I neurons,
@@ -682,186 +581,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     if (nU == 0) {
       // no valid expert at all: the CTA's output rows are zero
       for (int r = dw.r0 + ctid; r < dw.r1; r += ncons) p.y[r] = 0;
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Gate/up for several tokens with x staged in shared memory (T >= 2 when the
-// T tokens' x fits): the work units and token groups of
-// moe_gate_up_3d_batched, but each CTA converts x once to f16 blocks scaled
-// by a power of two (as the one-launch kernel does), each weight block is
-// decoded once to f16 pairs for all of a group's tokens, and fma.rn.f32.f16
-// forms every product (exact, as the header explains).
-// ---------------------------------------------------------------------------
-
-constexpr int kXsWarps = 16;
-constexpr int kXsThreads = kXsWarps * 32;
-
-// Shared-memory bytes of moe_gate_up_xs for T tokens of H (all of it dynamic:
-// the warps' schedule words, then x as f16 blocks, then their factors).
-__host__ __device__ constexpr size_t gate_up_xs_smem(int T, int H) {
-  return (size_t)kXsWarps * 32 * 4 + (size_t)T * (H >> 5) * (64 + 4);
-}
-
-// Four E4M3 codes (one word) -> two f16x2 words: elements 0,1 and 2,3.
-__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t codes, uint32_t& w01, uint32_t& w23) {
-  asm("{\n\t.reg .b16 c0, c1;\n\tmov.b32 {c0, c1}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, c0;\n\tcvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
-      : "=r"(w01), "=r"(w23)
-      : "r"(codes));
-}
-
-// Four products of f16 pairs (weights w01, w23 against activations x01, x23)
-// added to two FP32 accumulators.
-__device__ __forceinline__ void fma_f16x4(float& p, float& q, uint32_t w01, uint32_t w23,
-                                          uint32_t x01, uint32_t x23) {
-  asm("{\n\t.reg .f16 w0, w1, w2, w3, v0, v1, v2, v3;\n\t"
-      "mov.b32 {w0, w1}, %2;\n\tmov.b32 {w2, w3}, %3;\n\t"
-      "mov.b32 {v0, v1}, %4;\n\tmov.b32 {v2, v3}, %5;\n\t"
-      "fma.rn.f32.f16 %0, w0, v0, %0;\n\tfma.rn.f32.f16 %1, w1, v1, %1;\n\t"
-      "fma.rn.f32.f16 %0, w2, v2, %0;\n\tfma.rn.f32.f16 %1, w3, v3, %1;\n\t}"
-      : "+f"(p), "+f"(q)
-      : "r"(w01), "r"(w23), "r"(x01), "r"(x23));
-}
-
-// One weight block (32 codes in q, this lane's half first when LaneBlock says
-// so) decoded to 16 f16x2 words in that order.
-__device__ __forceinline__ void decode_block_f16(const uint32_t (&q)[8], bool swap,
-                                                 uint32_t (&wh)[16]) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint32_t v = swap ? q[c ^ 4] : q[c];
-    e4m3x4_to_f16x2(v, wh[2 * c], wh[2 * c + 1]);
-  }
-}
-
-// The block dot of decoded weights against the f16 activation block at act.
-__device__ __forceinline__ float dot_block_h(const uint32_t (&wh)[16], const uint8_t* act,
-                                             const LaneBlock& lb) {
-  const uint4 x0 = *reinterpret_cast<const uint4*>(act + lb.x0);
-  const uint4 x1 = *reinterpret_cast<const uint4*>(act + lb.x1);
-  const uint4 x2 = *reinterpret_cast<const uint4*>(act + lb.x2);
-  const uint4 x3 = *reinterpret_cast<const uint4*>(act + lb.x3);
-  float p = 0.f, q = 0.f, r = 0.f, s = 0.f;
-  fma_f16x4(p, q, wh[0], wh[1], x0.x, x0.y);
-  fma_f16x4(p, q, wh[2], wh[3], x0.z, x0.w);
-  fma_f16x4(p, q, wh[4], wh[5], x1.x, x1.y);
-  fma_f16x4(p, q, wh[6], wh[7], x1.z, x1.w);
-  fma_f16x4(r, s, wh[8], wh[9], x2.x, x2.y);
-  fma_f16x4(r, s, wh[10], wh[11], x2.z, x2.w);
-  fma_f16x4(r, s, wh[12], wh[13], x3.x, x3.y);
-  fma_f16x4(r, s, wh[14], wh[15], x3.z, x3.w);
-  return (p + q) + (r + s);
-}
-
-template <int NT, int KMAX>
-__global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_xs(GateUpParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int lane = threadIdx.x & 31;
-  const int wid = threadIdx.x >> 5;
-  const int H = p.H, I = p.I, nb = H >> 5;
-  uint32_t* sm_words = reinterpret_cast<uint32_t*>(smem);              // [warps][32]
-  uint8_t* xs = smem + kXsWarps * 32 * 4;                              // [T][nb] x blocks
-  float* xf = reinterpret_cast<float*>(xs + (size_t)p.T * nb * 64);    // [T][nb] factors
-  pdl_wait();      // x and topk_ids come from upstream work
-  pdl_trigger();   // the down kernel may start fetching its weights
-  WarpSchedule<KMAX> s;
-  s.load(p.ids, p.T, p.k);
-  // x -> f16 blocks while the ids are in flight
-#pragma unroll 1
-  for (int idx = threadIdx.x; idx < p.T * nb; idx += kXsThreads) {
-    const int t = idx / nb, b = idx - t * nb;
-    const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * H) + 4 * b;
-    const uint4 v[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3)};
-    xf[idx] = stage_block_f16(v, xs + 64 * idx, b);
-  }
-  s.finish(p.E, sm_words + wid * 32, p.err);
-  // A slot with an out-of-range id gets no unit; its h slice is defined as zero.
-  if (__any_sync(kFull, s.badmask != 0u)) {
-    for (int t = blockIdx.x * kXsWarps + wid; t < p.T; t += gridDim.x * kXsWarps) {
-      const uint32_t bm = __shfl_sync(kFull, s.badmask, t);
-      for (uint32_t m = bm; m; m &= m - 1) {
-        uint16_t* row = p.h + ((size_t)t * p.k + (__ffs(m) - 1)) * I;
-        for (int i = lane; i < I; i += 32) row[i] = 0;
-      }
-    }
-  }
-  __syncthreads();   // x staged
-  const LaneBlock lb(lane);
-  const bool swap = lb.c_first != 0;
-  const long long units = (long long)s.n_unique * I;
-#pragma unroll 1
-  for (long long unit = (long long)blockIdx.x * kXsWarps + wid; unit < units;
-       unit += (long long)gridDim.x * kXsWarps) {
-    const int u = (int)(unit / I);
-    const int i = (int)(unit - (long long)u * I);
-    const int e = s.expert(u);
-    const uint32_t jm = s.jmask(e);
-    uint32_t tokens = __ballot_sync(kFull, jm != 0u);
-    const size_t row = (size_t)e * 2 * I + i;
-    const uint8_t* wg = p.wgu + row * H;
-    const uint8_t* wu = wg + (size_t)I * H;
-    const uint8_t* sg = p.sgu + row * nb;
-    const uint8_t* su = sg + (size_t)I * nb;
-#pragma unroll 1
-    while (tokens) {
-      int tok[NT];
-      int nt = 0;
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        tok[n] = tokens ? __ffs(tokens) - 1 : 0;
-        if (tokens) {
-          tokens &= tokens - 1;
-          ++nt;
-        }
-      }
-      float ag[NT], au[NT];
-#pragma unroll
-      for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
-      // the next block's codes are in flight while this one is applied
-      uint32_t qg[8], qu[8];
-      uint32_t s_g = 0, s_u = 0;
-      int b = lane;
-      if (b < nb) {
-        ld_weights32(wg + b * 32, qg);
-        ld_weights32(wu + b * 32, qu);
-        s_g = ld_scale(sg + b);
-        s_u = ld_scale(su + b);
-      }
-#pragma unroll 1
-      for (; b < nb; b += 32) {
-        uint32_t whg[16], whu[16];
-        decode_block_f16(qg, swap, whg);
-        decode_block_f16(qu, swap, whu);
-        const float scg = ue8m0_to_f32(s_g), scu = ue8m0_to_f32(s_u);
-        if (b + 32 < nb) {
-          ld_weights32(wg + (b + 32) * 32, qg);
-          ld_weights32(wu + (b + 32) * 32, qu);
-          s_g = ld_scale(sg + b + 32);
-          s_u = ld_scale(su + b + 32);
-        }
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          if (n < nt) {
-            const int xb = tok[n] * nb + b;
-            const uint8_t* act = xs + 64 * xb;
-            const float fx = xf[xb];
-            ag[n] = fmaf(dot_block_h(whg, act, lb) * fx, scg, ag[n]);
-            au[n] = fmaf(dot_block_h(whu, act, lb) * fx, scu, au[n]);
-          }
-        }
-      }
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        if (n < nt) {
-          const float g = warp_sum(ag[n]);
-          const float up = warp_sum(au[n]);
-          const uint32_t jt = __shfl_sync(kFull, jm, tok[n]);
-          const uint16_t hb = f32_to_bf16_rn((g / (1.0f + expf(-g))) * up);
-          if (lane < p.k && ((jt >> lane) & 1u)) p.h[((size_t)tok[n] * p.k + lane) * I + i] = hb;
-        }
-      }
     }
   }
 }
