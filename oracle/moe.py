@@ -38,6 +38,7 @@ from typing import Callable, Mapping
 import numpy as np
 
 from .bf16 import bf16_rne
+from .mxfp4 import dequantize as dequantize_mxfp4
 from .mxfp8 import E4M3, dequantize
 
 ExpertSource = Mapping[int, tuple] | Callable[[int], tuple]
@@ -45,6 +46,16 @@ ExpertSource = Mapping[int, tuple] | Callable[[int], tuple]
 
 def _get(experts: ExpertSource, e: int):
     return experts(e) if callable(experts) else experts[e]
+
+
+# Weight formats: MXFP8 (E4M3 codes, one byte each) and MXFP4 (E2M1 codes,
+# two to a byte); both carry one UE8M0 scale per 32 elements along K.
+def _dq(fmt: str):
+    if fmt == "mxfp8":
+        return dequantize
+    if fmt == "mxfp4":
+        return dequantize_mxfp4
+    raise ValueError(f"unknown weight format {fmt!r}")
 
 
 def silu(z) -> np.ndarray:
@@ -118,14 +129,16 @@ def _slots_by_expert(ids: np.ndarray, E: int, tokens) -> dict[int, list[tuple[in
 
 
 def gate_up(x: np.ndarray, ids: np.ndarray, experts: ExpertSource, E: int, I: int,
-            tokens=None) -> tuple[np.ndarray, np.ndarray]:
+            tokens=None, fmt: str = "mxfp8") -> tuple[np.ndarray, np.ndarray]:
     """h[t, j, :] = SiLU(dq(Wg_e) x_t) * (dq(Wu_e) x_t), e = ids[t, j].
 
     x: float64 [T, H] holding the bf16 input values exactly.
     Returns (h_spec, h_pure), float64 [T, k, I]; h_spec is rounded to bf16.
     `tokens` restricts the work to a subset of tokens (other rows stay zero).
     Each expert is dequantised once and released after its slots are done.
+    `fmt` names the weight format ("mxfp8" or "mxfp4").
     """
+    dequantize = _dq(fmt)
     x = np.asarray(x, dtype=np.float64)
     ids = np.asarray(ids)
     T, k = ids.shape
@@ -142,12 +155,13 @@ def gate_up(x: np.ndarray, ids: np.ndarray, experts: ExpertSource, E: int, I: in
 
 
 def down(h: np.ndarray, ids: np.ndarray, w: np.ndarray, experts: ExpertSource, E: int,
-         H: int, tokens=None, rows=None) -> np.ndarray:
+         H: int, tokens=None, rows=None, fmt: str = "mxfp8") -> np.ndarray:
     """y[t, r] = sum_j w[t, j] * (dq(Wd_e)[r, :] . h[t, j, :]), e = ids[t, j].
 
     h: float64 [T, k, I]; w: float32 [T, k] (used at its exact value).
     Returns float64 [T, H] (or [T, len(rows)]), not rounded.
     """
+    dequantize = _dq(fmt)
     h = np.asarray(h, dtype=np.float64)
     ids = np.asarray(ids)
     wt = np.asarray(w, dtype=np.float32).astype(np.float64)
@@ -163,11 +177,12 @@ def down(h: np.ndarray, ids: np.ndarray, w: np.ndarray, experts: ExpertSource, E
     return terms.sum(axis=1)
 
 
-def layer(x, ids, w, experts: ExpertSource, E: int, H: int, I: int, tokens=None, rows=None):
+def layer(x, ids, w, experts: ExpertSource, E: int, H: int, I: int, tokens=None, rows=None,
+          fmt: str = "mxfp8"):
     """The whole layer: h_spec, h_pure, y_spec (from bf16 h), y_pure (from exact h)."""
-    h_spec, h_pure = gate_up(x, ids, experts, E, I, tokens=tokens)
-    y_spec = down(h_spec, ids, w, experts, E, H, tokens=tokens, rows=rows)
-    y_pure = down(h_pure, ids, w, experts, E, H, tokens=tokens, rows=rows)
+    h_spec, h_pure = gate_up(x, ids, experts, E, I, tokens=tokens, fmt=fmt)
+    y_spec = down(h_spec, ids, w, experts, E, H, tokens=tokens, rows=rows, fmt=fmt)
+    y_pure = down(h_pure, ids, w, experts, E, H, tokens=tokens, rows=rows, fmt=fmt)
     return {"h_spec": h_spec, "h_pure": h_pure, "y_spec": y_spec, "y_pure": y_pure}
 
 
@@ -216,7 +231,8 @@ def requantize_mxfp8(a: np.ndarray) -> np.ndarray:
     return np.ldexp(_round_e4m3(q), e[..., None]).reshape(a.shape)
 
 
-def layer_classic(x, ids, w, experts: ExpertSource, E: int, H: int, I: int, tokens=None):
+def layer_classic(x, ids, w, experts: ExpertSource, E: int, H: int, I: int, tokens=None,
+                  fmt: str = "mxfp8"):
     """Layer output when h is quantised to MXFP8 before the down projection."""
-    h_spec, _ = gate_up(x, ids, experts, E, I, tokens=tokens)
-    return down(requantize_mxfp8(h_spec), ids, w, experts, E, H, tokens=tokens)
+    h_spec, _ = gate_up(x, ids, experts, E, I, tokens=tokens, fmt=fmt)
+    return down(requantize_mxfp8(h_spec), ids, w, experts, E, H, tokens=tokens, fmt=fmt)

@@ -353,11 +353,11 @@ def test_brute_force_catches_planted_mistakes(monkeypatch):
 def test_brute_force_catches_swapped_gate_up(monkeypatch):
     real = om.gate_up
 
-    def swapped(x, ids, experts, E, I, tokens=None):
+    def swapped(x, ids, experts, E, I, tokens=None, fmt="mxfp8"):
         def src(e):
             wgu, sgu, wd, sd = experts[e]
             return (np.concatenate([wgu[I:], wgu[:I]]), np.concatenate([sgu[I:], sgu[:I]]), wd, sd)
-        return real(x, ids, src, E, I, tokens=tokens)
+        return real(x, ids, src, E, I, tokens=tokens, fmt=fmt)
 
     monkeypatch.setattr(om, "gate_up", swapped)
     assert not _brute_agrees()
@@ -366,8 +366,9 @@ def test_brute_force_catches_swapped_gate_up(monkeypatch):
 def test_brute_force_catches_misapplied_routing_weight(monkeypatch):
     real = om.down
 
-    def wrong(h, ids, w, experts, E, H, tokens=None, rows=None):
-        return real(h, ids, np.asarray(w)[:, ::-1].copy(), experts, E, H, tokens=tokens, rows=rows)
+    def wrong(h, ids, w, experts, E, H, tokens=None, rows=None, fmt="mxfp8"):
+        return real(h, ids, np.asarray(w)[:, ::-1].copy(), experts, E, H, tokens=tokens, rows=rows,
+                    fmt=fmt)
 
     monkeypatch.setattr(om, "down", wrong)
     assert not _brute_agrees()

@@ -32,6 +32,16 @@ shared exponent = floor(log2(amax)) - 8 clamped to [-127, 127] (scale code =
 exponent + 127; an all-zero block gets code 127), elements divided by 2^exp,
 saturated to +-448 and rounded to the nearest E4M3 value (ties to even). It
 never emits a NaN code.
+
+The MXFP4 variant of every workload draws the same float weights and stores
+them as E2M1 codes, two to a byte (element 2c in the low nibble of byte c,
+element 2c+1 in the high nibble), with the same UE8M0 scale layout (the
+routed-weight format the GC-MoE summary, "How it is used", names for
+Blackwell). Its encoder follows the same MX recipe with E2M1's largest
+exponent: shared exponent = floor(log2(amax)) - 2, elements divided by 2^exp,
+saturated to +-6 and rounded to the nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6
+(ties to the even code); the sign bit follows the element's sign, so small
+negative elements become -0.
 """
 from __future__ import annotations
 
@@ -44,7 +54,8 @@ import torch
 
 __all__ = [
     "Workload", "WORKLOADS", "workload", "seed_of",
-    "make_x", "make_logits", "encode_mxfp8", "make_expert", "make_experts",
+    "make_x", "make_logits", "encode_mxfp8", "encode_mxfp4", "make_expert", "make_experts",
+    "FORMATS",
     "bf16_bits_to_f64", "NAN_CODE",
 ]
 
@@ -67,7 +78,12 @@ class Workload:
     @property
     def weight_bytes_per_expert(self) -> int:
         """E4M3 codes plus UE8M0 scales of one expert's three projections."""
-        return 3 * self.H * self.I + 3 * self.H * self.I // 32
+        return self.weight_bytes("mxfp8")
+
+    def weight_bytes(self, fmt: str = "mxfp8") -> int:
+        """Codes plus UE8M0 scales of one expert's three projections in `fmt`."""
+        codes = 3 * self.H * self.I
+        return (codes if fmt == "mxfp8" else codes // 2) + codes // 32
 
 
 WORKLOADS = {
@@ -139,22 +155,55 @@ def encode_mxfp8(w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return codes, scales
 
 
-def make_expert(w: Workload, seed: int, e: int):
-    """One expert's MXFP8 tensors: (wgu [2I,H], sgu [2I,H/32], wd [H,I], sd [H,I/32])."""
+# magnitudes of the E2M1 codes 0..7, the rounding targets of encode_mxfp4
+_E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
+
+
+def encode_mxfp4(w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """float32 [R, K] (K % 32 == 0) -> (packed E2M1 codes uint8 [R, K/2], UE8M0 codes uint8 [R, K/32])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    R, K = w.shape
+    assert K % 32 == 0
+    b = w.reshape(R, K // 32, 32).astype(np.float64)
+    amax = np.abs(b).max(axis=-1)
+    _, ex = np.frexp(amax)                         # amax = m * 2^ex, m in [0.5, 1)
+    e = np.clip(ex - 1 - 2, -127, 127)             # floor(log2 amax) - 2
+    e = np.where(amax == 0, 0, e)
+    q = np.ldexp(b, -e[..., None])
+    a = np.minimum(np.abs(q), 6.0)
+    hi = np.clip(np.searchsorted(_E2M1_GRID, a, side="left"), 0, 7)
+    lo = np.clip(hi - 1, 0, 7)
+    dlo, dhi = a - _E2M1_GRID[lo], _E2M1_GRID[hi] - a
+    mag = np.where((dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0)), hi, lo)
+    codes = (mag | (np.signbit(q).astype(np.int64) << 3)).astype(np.uint8).reshape(R, K)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    scales = (e + 127).astype(np.uint8)
+    return packed, scales
+
+
+FORMATS = {"mxfp8": encode_mxfp8, "mxfp4": encode_mxfp4}
+
+
+def make_expert(w: Workload, seed: int, e: int, fmt: str = "mxfp8"):
+    """One expert's weight tensors in `fmt` ("mxfp8" or "mxfp4"):
+    (wgu [2I, H*c], sgu [2I, H/32], wd [H, I*c], sd [H, I/32]), c = 1 code
+    byte per element for MXFP8 and 1/2 for MXFP4."""
+    enc = FORMATS[fmt]
     gu = _rng(seed, 3, e).standard_normal((2 * w.I, w.H), dtype=np.float32)
     gu *= np.float32(w.sigma)
-    wgu, sgu = encode_mxfp8(gu)
+    wgu, sgu = enc(gu)
     del gu
     dn = _rng(seed, 4, e).standard_normal((w.H, w.I), dtype=np.float32)
     dn *= np.float32(w.sigma)
-    wd, sd = encode_mxfp8(dn)
+    wd, sd = enc(dn)
     return wgu, sgu, wd, sd
 
 
-def make_experts(w: Workload, seed: int, experts, threads: int | None = None) -> dict:
-    """{e: make_expert(w, seed, e)} for the given expert ids, generated in parallel."""
+def make_experts(w: Workload, seed: int, experts, threads: int | None = None,
+                 fmt: str = "mxfp8") -> dict:
+    """{e: make_expert(w, seed, e, fmt)} for the given expert ids, generated in parallel."""
     experts = sorted(set(int(e) for e in experts))
     threads = threads or min(16, os.cpu_count() or 1)
     with ThreadPoolExecutor(max_workers=threads) as ex:
-        out = list(ex.map(lambda e: make_expert(w, seed, e), experts))
+        out = list(ex.map(lambda e: make_expert(w, seed, e, fmt), experts))
     return dict(zip(experts, out))
