@@ -19,7 +19,8 @@ bounded sample of the same workload.
 
 --workload N runs one of the other configurations instead (0: tiny, 2: T=8,
 3: Zipf-skewed T=32, 4: large experts T=16), for reports; the default line is
-workload 1.
+workload 1. --format mxfp4 stores the same weights as MXFP4 (E2M1 codes two
+to a byte, the same UE8M0 scales): half the code bytes per step.
 """
 from __future__ import annotations
 
@@ -61,6 +62,7 @@ def parse():
     ap.add_argument("--cpu-sample-s", type=float, default=12.0)
     # the other configurations, for reports (the default line is workload 1)
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--format", default="mxfp8", choices=sorted(wl.FORMATS))
     return ap.parse_args()
 
 
@@ -110,13 +112,18 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
+def traffic_key(kernel: str, workload: str, fmt: str) -> str:
+    return f"{kernel} | {workload} | {fmt}"
+
+
+def recorded_traffic(kernel: str, workload: str, fmt: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this
+    kernel, workload, weight format and source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    e = d.get(kernel)
+    e = d.get(traffic_key(kernel, workload, fmt))
     if not e or e.get("source_hash") != source_hash():
         return None
     return float(e["dram_bytes_per_launch_full"])
@@ -178,21 +185,21 @@ class ClockSampler:
 # reference arm / cpu baseline: the float64 oracle on host cores
 # ---------------------------------------------------------------------------
 
-def oracle_steps(w, seed, experts, n_steps, step0=0):
+def oracle_steps(w, seed, experts, n_steps, step0=0, fmt="mxfp8"):
     import oracle
     t0 = time.perf_counter()
     for s in range(n_steps):
         x = wl.bf16_bits_to_f64(wl.make_x(w, seed + 7919 * (step0 + s + 1), w.T))
         ids, tw = oracle.route(wl.make_logits(w, seed, w.T, step=step0 + s + 1), w.k)
-        oracle.layer(x, ids, tw, experts, w.E, w.H, w.I)
+        oracle.layer(x, ids, tw, experts, w.E, w.H, w.I, fmt=fmt)
     return time.perf_counter() - t0
 
 
-def cpu_oracle_rate(w, seed, experts, budget_s):
+def cpu_oracle_rate(w, seed, experts, budget_s, fmt="mxfp8"):
     """tokens/s of the oracle over as many steps as fit in ~budget_s (at least 2)."""
-    dt = oracle_steps(w, seed, experts, 1)
+    dt = oracle_steps(w, seed, experts, 1, fmt=fmt)
     n = max(2, int(budget_s / max(dt, 1e-3)))
-    dt = oracle_steps(w, seed, experts, n, step0=1)
+    dt = oracle_steps(w, seed, experts, n, step0=1, fmt=fmt)
     return w.T * n / dt, n, dt
 
 
@@ -206,18 +213,19 @@ def run_reference(args, rank, world):
 
     def experts(e):
         if e not in cache:
-            cache[e] = wl.make_expert(w, seed, e)
+            cache[e] = wl.make_expert(w, seed, e, fmt=args.format)
         return cache[e]
 
-    oracle_steps(w, seed, experts, args.warmup, step0=10_000)
-    dt = oracle_steps(w, seed, experts, args.steps, step0=20_000)
+    oracle_steps(w, seed, experts, args.warmup, step0=10_000, fmt=args.format)
+    dt = oracle_steps(w, seed, experts, args.steps, step0=20_000, fmt=args.format)
     v = w.T * args.steps / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "E": w.E, "k": w.k, "H": w.H, "I": w.I, "T": w.T},
+        "config": {"workload": w.name, "E": w.E, "k": w.k, "H": w.H, "I": w.I, "T": w.T,
+                   "weights": args.format},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} decode steps of the workload (fresh routing each), "
                                    "float64 numpy oracle, single thread"},
@@ -240,10 +248,13 @@ def run_ours(args, rank, world, local):
     K, W, L = args.steps, args.warmup, args.layers
     T, E, k, H, I = w.T, w.E, w.k, w.H, w.I
 
-    # one layer's MXFP8 weights, L resident copies at distinct addresses; a
-    # layer of several GB (workload 4) gets random MXFP8 bytes generated on the
-    # device instead (the timing does not depend on the values; no oracle leg)
-    big = w.E * w.weight_bytes_per_expert > 4e9
+    # one layer's weights, L resident copies at distinct addresses; a layer of
+    # several GB (workload 4) gets random code bytes generated on the device
+    # instead (the timing does not depend on the values; no oracle leg)
+    fmt = args.format
+    per = 2 if fmt == "mxfp4" else 1              # elements per code byte
+    expert_bytes = w.weight_bytes(fmt)
+    big = w.E * expert_bytes > 4e9
     if big:
         L = min(L, 2)
         gen = torch.Generator(device=dev)
@@ -251,21 +262,22 @@ def run_ours(args, rank, world, local):
 
         def codes(*shape):
             c = torch.randint(0, 0xFE, shape, dtype=torch.uint8, device=dev, generator=gen)
-            return c.masked_fill_(c == 0x7F, 0x7E)            # no NaN codes
+            return c.masked_fill_(c == 0x7F, 0x7E)            # no E4M3 NaN codes
 
         def scales(*shape):
             return torch.randint(118, 124, shape, dtype=torch.uint8, device=dev, generator=gen)
 
         experts = None
-        base = [codes(E, 2 * I, H), scales(E, 2 * I, H // 32), codes(E, H, I), scales(E, H, I // 32)]
+        base = [codes(E, 2 * I, H // per), scales(E, 2 * I, H // 32), codes(E, H, I // per),
+                scales(E, H, I // 32)]
     else:
-        experts = wl.make_experts(w, seed, range(E))
+        experts = wl.make_experts(w, seed, range(E), fmt=fmt)
         host = [np.stack([experts[e][i] for e in range(E)]) for i in range(4)]
         base = [torch.from_numpy(a).to(dev) for a in host]
     layers = []
     for _ in range(L):
         t = [b.clone() for b in base]
-        layers.append((t, MoEDecode(*t, k=k, max_T=T)))
+        layers.append((t, MoEDecode(*t, k=k, max_T=T, fmt=fmt)))
     del base
 
     # per-step activations and routing (routing by the library's router)
@@ -274,7 +286,7 @@ def run_ours(args, rank, world, local):
                              .view(np.int16)).view(torch.bfloat16).to(dev)
     logits = torch.from_numpy(np.stack([wl.make_logits(w, seed, T, step=s + 1) for s in range(nsteps)])
                               ).to(dev).view(nsteps * T, E)
-    router = MoEDecode(*layers[0][0], k=k, max_T=nsteps * T)
+    router = MoEDecode(*layers[0][0], k=k, max_T=nsteps * T, fmt=fmt)
     ids_all, w_all = router.route(logits)
     ids_all = ids_all.view(nsteps, T, k)
     w_all = w_all.view(nsteps, T, k)
@@ -282,11 +294,12 @@ def run_ours(args, rank, world, local):
     y = torch.empty((nsteps, T, H), dtype=torch.bfloat16, device=dev)
     torch.cuda.synchronize()
 
-    # algorithmic weight bytes per step: unique routed experts x 3HI x 33/32
+    # algorithmic weight bytes per step: unique routed experts x their codes
+    # and scales (3HI x 33/32 for MXFP8, 3HI x 17/32 for MXFP4)
     ids_np = ids_all.cpu().numpy()
     uniq = np.array([len(np.unique(ids_np[s])) for s in range(nsteps)])
-    bytes_step = uniq * w.weight_bytes_per_expert
-    bytes_gu = uniq * (2 * I * H + 2 * I * H // 32)
+    bytes_step = uniq * expert_bytes
+    bytes_gu = uniq * (2 * I * H // per + 2 * I * H // 32)
 
     def step(s, only_gate_up=False):
         lay = layers[s % L][1]
@@ -358,7 +371,7 @@ def run_ours(args, rank, world, local):
         launch_s = dt_gu / K
         achieved = float(bytes_gu[W:].mean()) / launch_s / 1e9
         launches = 2 * K
-    traffic = recorded_traffic(kernel)
+    traffic = recorded_traffic(kernel, w.name, fmt)
 
     # end to end through the host-buffer entry point, every step: the step's
     # pinned host inputs go to the device (read in place by the kernels
@@ -368,7 +381,7 @@ def run_ours(args, rank, world, local):
     ih = ids_all.cpu().pin_memory()
     wh = w_all.cpu().pin_memory()
     yh = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    e2e_layers = [MoEDecode(*t, k=k, max_T=T) for t, _ in layers]
+    e2e_layers = [MoEDecode(*t, k=k, max_T=T, fmt=fmt) for t, _ in layers]
     for s in range(min(W, 10)):
         e2e_layers[s % L].forward_host(xh[s], ih[s], wh[s], yh)
     barrier(world)
@@ -385,7 +398,7 @@ def run_ours(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and experts is not None:
-        r, n, cdt = cpu_oracle_rate(w, seed, experts, args.cpu_sample_s)
+        r, n, cdt = cpu_oracle_rate(w, seed, experts, args.cpu_sample_s, fmt=fmt)
         cpu = {"value": r, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} decode steps of the workload (T={T}, fresh routing each), "
                          f"{cdt:.1f} s of float64 numpy on one host thread"}
@@ -399,11 +412,13 @@ def run_ours(args, rank, world, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {
                 "workload": w.name, "E": E, "k": k, "H": H, "I": I, "T": T,
-                "weights": "MXFP8 (E4M3 + UE8M0 per 32), bf16 activations, FP32 accumulate"
+                "weights": ("MXFP4 (E2M1 two per byte + UE8M0 per 32)" if fmt == "mxfp4" else
+                            "MXFP8 (E4M3 + UE8M0 per 32)")
+                           + ", bf16 activations, FP32 accumulate"
                            + (" (random bytes generated on the device: timing only)" if big else ""),
                 "layers_rotated": L,
                 "l2": f"inputs larger than L2: {L} resident layer copies "
-                      f"({L * w.E * w.weight_bytes_per_expert / 1e9:.1f} GB) with fresh routing "
+                      f"({L * w.E * expert_bytes / 1e9:.1f} GB) with fresh routing "
                       "and activations every step",
                 "timing": "one CUDA-graph replay of K steps, CUDA events on the replay stream",
                 "parallelism": f"replicas x{world}",

@@ -16,8 +16,12 @@
  * dq() is MXFP8 dequantisation: one E4M3 code per element and one UE8M0
  * exponent per 32 consecutive elements along the reduction axis (the block
  * format named in the GC-MoE summary, onedev.kr/papers/1690, "How it is
- * used"): dq = E4M3(code) * 2^(scale - 127). Dot products accumulate in FP32;
- * h and y are rounded to BF16 (round to nearest even).
+ * used"): dq = E4M3(code) * 2^(scale - 127). With MOE_FLAG_MXFP4 it is MXFP4
+ * dequantisation instead, the routed-weight format of the same page and
+ * section: one E2M1 code per element (1 sign, 2 exponent bits with bias 1,
+ * 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), two codes to a
+ * byte, with the same UE8M0 scales. Dot products accumulate in FP32; h and y
+ * are rounded to BF16 (round to nearest even).
  *
  * Conventions shared by every call:
  *   - Tensors are row-major and contiguous. bf16 tensors are passed as
@@ -65,6 +69,8 @@ typedef enum {
 #define MOE_FLAG_NO_PDL 0x1u       /* launch without programmatic dependent launch */
 #define MOE_FLAG_HOST_COPY 0x2u    /* moe_decode_forward_host always copies through
                                       the device staging buffers */
+#define MOE_FLAG_MXFP4 0x4u        /* the weights are MXFP4, not MXFP8 (see
+                                      moe_decode_create) */
 
 typedef struct {
   int32_t E;      /* experts, 1..1024 */
@@ -84,9 +90,12 @@ typedef struct moe_decode* moe_decode_t;
  *   s_gateup  device uint8 [E, 2I, H/32] UE8M0 scale codes
  *   w_down    device uint8 [E, H, I]    E4M3 codes
  *   s_down    device uint8 [E, H, I/32] UE8M0 scale codes
- * w_gateup and w_down must be 32-byte aligned (rows are then 32-byte aligned
- * too); the scale arrays need no alignment (16-byte aligned scale arrays
- * enable the one-launch single-token layer). Allocates 32 bytes of device
+ * With MOE_FLAG_MXFP4 in cfg->flags, w_gateup is uint8 [E, 2I, H/2] and
+ * w_down uint8 [E, H, I/2]: E2M1 codes, element 2c of a row in the low
+ * nibble of byte c and element 2c+1 in its high nibble; the scales are as
+ * above. w_gateup and w_down must be 32-byte aligned; the scale arrays need
+ * no alignment (16-byte aligned scale arrays enable the one-launch
+ * single-token layer, which with MXFP4 also needs H a multiple of 1024). Allocates 32 bytes of device
  * state (the error word and the one-launch kernel's launch and grid-barrier
  * counters) and, when max_T > 0, the staging buffers of
  * moe_decode_forward_host. *out receives the handle; on error *out is NULL.
@@ -206,8 +215,8 @@ int32_t moe_decode_version(void);
  * launch (both projections in one cooperative kernel, TMA-streamed weights,
  * a grid barrier between them) for this handle, 0 when it falls back to the
  * two kernels (shape or alignment outside that kernel's limits: H a multiple
- * of 512, I a multiple of 128, scale arrays 16-byte aligned, enough shared
- * memory), -1 for a NULL handle.
+ * of 512 (of 1024 with MOE_FLAG_MXFP4), I a multiple of 128, scale arrays
+ * 16-byte aligned, enough shared memory), -1 for a NULL handle.
  */
 int32_t moe_decode_fused_layer(moe_decode_t handle);
 

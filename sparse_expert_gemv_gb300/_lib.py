@@ -17,6 +17,7 @@ MOE_DEVICE_BAD_ID = 0x1
 MOE_DEVICE_TIMEOUT = 0x2
 MOE_FLAG_NO_PDL = 0x1
 MOE_FLAG_HOST_COPY = 0x2
+MOE_FLAG_MXFP4 = 0x4
 MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 STATUS_NAMES = {

@@ -87,9 +87,15 @@ cudaError_t launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream
 
 bool use_pdl(const moe_decode* m) { return (m->cfg.flags & MOE_FLAG_NO_PDL) == 0; }
 
+// The handle's weight format: MXFP4 (E2M1 codes, two to a byte) or MXFP8.
+bool is_fp4(const moe_decode* m) { return (m->cfg.flags & MOE_FLAG_MXFP4) != 0; }
+int code_bytes_per_block(const moe_decode* m) { return is_fp4(m) ? 16 : 32; }
+
+constexpr uint32_t kKnownFlags = MOE_FLAG_NO_PDL | MOE_FLAG_HOST_COPY | MOE_FLAG_MXFP4;
+
 // ---- gate/up ---------------------------------------------------------------
 
-template <int NT, int KMAX>
+template <int NT, int KMAX, class F>
 cudaError_t launch_gate_up_t(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
   // several tokens whose x fits in shared memory: staged once per CTA as f16
   // blocks (one 16-warp CTA per SM)
@@ -98,28 +104,33 @@ cudaError_t launch_gate_up_t(const moe_decode* m, const moe::GateUpParams& p, cu
     const long long units_max = (long long)std::min(p.E, p.T * p.k) * p.I;
     const long long ctas_needed = (units_max + moe::kXsWarps - 1) / moe::kXsWarps;
     const int grid = (int)std::max(1LL, std::min(ctas_needed, (long long)m->num_sms));
-    return launch(moe::moe_gate_up_3d_batched_xs<NT, KMAX>, dim3(grid), dim3(moe::kXsThreads), xs, s,
-                  use_pdl(m), p);
+    return launch(moe::moe_gate_up_3d_batched_xs<NT, KMAX, F>, dim3(grid), dim3(moe::kXsThreads), xs,
+                  s, use_pdl(m), p);
   }
   const long long units_max = (long long)std::min(p.E, p.T * p.k) * p.I;
   const long long ctas_needed = (units_max + moe::kWarps - 1) / moe::kWarps;
   const long long cap = (long long)m->num_sms * m->gate_up_ctas_per_sm;
   const int grid = (int)std::max(1LL, std::min(ctas_needed, cap));
-  return launch(moe::moe_gate_up_3d_batched<NT, KMAX>, dim3(grid), dim3(moe::kThreads), 0, s,
+  return launch(moe::moe_gate_up_3d_batched<NT, KMAX, F>, dim3(grid), dim3(moe::kThreads), 0, s,
                 use_pdl(m), p);
 }
 
-template <int KMAX>
+template <int KMAX, class F>
 cudaError_t launch_gate_up_k(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
-  if (p.T <= 1) return launch_gate_up_t<1, KMAX>(m, p, s);
-  if (p.T <= 2) return launch_gate_up_t<2, KMAX>(m, p, s);
-  if (p.T <= 4) return launch_gate_up_t<4, KMAX>(m, p, s);
-  return launch_gate_up_t<8, KMAX>(m, p, s);
+  if (p.T <= 1) return launch_gate_up_t<1, KMAX, F>(m, p, s);
+  if (p.T <= 2) return launch_gate_up_t<2, KMAX, F>(m, p, s);
+  if (p.T <= 4) return launch_gate_up_t<4, KMAX, F>(m, p, s);
+  return launch_gate_up_t<8, KMAX, F>(m, p, s);
+}
+
+template <class F>
+cudaError_t launch_gate_up_f(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
+  if (p.k <= 8) return launch_gate_up_k<8, F>(m, p, s);
+  return launch_gate_up_k<32, F>(m, p, s);
 }
 
 cudaError_t launch_gate_up(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
-  if (p.k <= 8) return launch_gate_up_k<8>(m, p, s);
-  return launch_gate_up_k<32>(m, p, s);
+  return is_fp4(m) ? launch_gate_up_f<moe::Mxfp4>(m, p, s) : launch_gate_up_f<moe::Mxfp8>(m, p, s);
 }
 
 // ---- down ------------------------------------------------------------------
@@ -127,8 +138,22 @@ cudaError_t launch_gate_up(const moe_decode* m, const moe::GateUpParams& p, cuda
 constexpr int kDownQ = 8;
 
 cudaError_t launch_down(const moe_decode* m, const moe::DownParams& p, cudaStream_t s) {
-  return launch(moe::moe_down_3d_batched<kDownQ>, dim3(p.H / moe::kWarps, p.T), dim3(moe::kThreads),
-                moe::down_xs_smem(p.k, p.I), s, use_pdl(m), p);
+  const dim3 grid(p.H / moe::kWarps, p.T), block(moe::kThreads);
+  const size_t smem = moe::down_xs_smem(p.k, p.I);
+  if (is_fp4(m))
+    return launch(moe::moe_down_3d_batched<kDownQ, moe::Mxfp4>, grid, block, smem, s, use_pdl(m), p);
+  return launch(moe::moe_down_3d_batched<kDownQ, moe::Mxfp8>, grid, block, smem, s, use_pdl(m), p);
+}
+
+// The down kernels' shared-memory limit: one value for every handle, the
+// library's maximum.
+cudaError_t set_down_attributes() {
+  cudaError_t e = cudaSuccess;
+  for (const void* f : {(const void*)moe::moe_down_3d_batched<kDownQ, moe::Mxfp8>,
+                        (const void*)moe::moe_down_3d_batched<kDownQ, moe::Mxfp4>})
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDownSmem);
+  return e;
 }
 
 // ---- single-token fused layer ----------------------------------------------
@@ -143,22 +168,24 @@ bool plan_fused(const moe_decode* m, moe::FusedParams& fp, size_t& smem) {
   const moe_decode_config_t& c = m->cfg;
   if (!m->fused_ok || c.H % 512 || c.I % 128 || !aligned(m->sgu, 16) || !aligned(m->sd, 16))
     return false;
-  const int nbI = c.I / 32;
+  const int CB = code_bytes_per_block(m);
+  const int nbI = c.I / 32, IB = nbI * CB;
   const int RG = 16 / gcd_int(16, nbI);
   if (c.H % RG) return false;
   const int rows_cta = (c.H / RG + m->num_sms - 1) / m->num_sms * RG;
   constexpr int kMaxSlots = 16;
-  // a stage's K-chunk: the first of these that H allows and the ring holds
-  // (1024-code stages put the first tiles to work sooner than whole 2 KB rows
-  // and free ring slots for the down rows earlier)
-  for (const int KC : {1024, 2048, 512}) {
+  // a stage's K-chunk, by its code bytes per row: the first of these that H
+  // allows and the ring holds (1 KB stages put the first tiles to work sooner
+  // than 2 KB ones and free ring slots for the down rows earlier)
+  for (const int KB : {1024, 2048, 512}) {
+    const int KC = KB / CB * 32;
     if (c.H % KC) continue;
-    const int slot_g = moe::GuStageLayout(KC).end;        // a multiple of 128
+    const int slot_g = moe::GuStageLayout(KB, KC).end;    // a multiple of 128
     // down row chunks of RC rows, as many as the consumers cover and a slot holds
     int RC = std::min(rows_cta, moe::kFusedConsumers / RG * RG);
-    while (RC >= RG && moe::round128(RC * (c.I + nbI)) > slot_g) RC -= RG;
+    while (RC >= RG && moe::round128(RC * (IB + nbI)) > slot_g) RC -= RG;
     if (RC < RG) continue;
-    const int slot_d = moe::round128(RC * (c.I + nbI));
+    const int slot_d = moe::round128(RC * (IB + nbI));
     const int SR = slot_g / slot_d;
     auto bytes = [&](int SG) { return (size_t)moe::FusedSmem(SG, slot_g, c.H, c.I, c.k).total; };
     if (bytes(2) > m->smem_per_block) continue;
@@ -168,7 +195,7 @@ bool plan_fused(const moe_decode* m, moe::FusedParams& fp, size_t& smem) {
     if ((c.k + SR - 1) / SR > SG) continue;
     smem = bytes(SG);
     fp.KC = KC;
-    fp.kin = std::min(256, KC / 4);
+    fp.kin = std::min(256, KB / 4);
     fp.SG = SG;
     fp.slot_g = slot_g;
     fp.SR = SR;
@@ -176,7 +203,7 @@ bool plan_fused(const moe_decode* m, moe::FusedParams& fp, size_t& smem) {
     fp.RG = RG;
     fp.RC = RC;
     fp.nkc = c.H / KC;
-    fp.kdiv = KC / (4 * fp.kin);
+    fp.kdiv = KB / (4 * fp.kin);
     fp.nrg = c.H / RG;
     return true;
   }
@@ -243,29 +270,35 @@ bool encode_u32_4d(CUtensorMap* tm, const void* base, uint64_t n0, uint64_t n1, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The fused kernel's tensor maps. W_gateup codes as [E*2I][H/(4*kin)][kin]
-// uint32 with boxes of kFusedNeurons rows x KC codes, its scales as
+// The fused kernel's tensor maps (code bytes per row: RB = H*CB/32 for
+// W_gateup, IB = I*CB/32 for W_down, KB = KC*CB/32 per K-chunk, CB the code
+// bytes of a 32-element block). W_gateup codes as [E*2I][RB/(4*kin)][kin]
+// uint32 with boxes of kFusedNeurons rows x KB bytes, its scales as
 // [E*2I][H/128] uint32 with boxes of kFusedNeurons rows x KC/32 scale bytes;
-// W_down codes as [E][H][I/(4*kin_d)][kin_d] uint32 with boxes of RC rows of
+// W_down codes as [E][H][IB/(4*kin_d)][kin_d] uint32 with boxes of RC rows of
 // one expert, its scales as [E][H*I/128] uint32 with boxes of RC rows.
 bool encode_fused_maps(moe_decode* m, int KC, int RC) {
   const moe_decode_config_t& c = m->cfg;
+  const int CB = code_bytes_per_block(m);
+  const int RB = c.H / 32 * CB, IB = c.I / 32 * CB, KB = KC / 32 * CB;
   const uint64_t rows = (uint64_t)c.E * 2 * c.I;
-  const int kin = std::min(256, KC / 4);
-  const int kin_d = std::min(256, c.I / 4);
-  return encode_u32_3d(&m->tm_codes, m->wgu, kin, c.H / (4 * kin), rows, c.H, KC / (4 * kin),
+  const int kin = std::min(256, KB / 4);
+  const int kin_d = std::min(256, IB / 4);
+  return encode_u32_3d(&m->tm_codes, m->wgu, kin, RB / (4 * kin), rows, RB, KB / (4 * kin),
                        moe::kFusedNeurons) &&
          encode_u32_2d(&m->tm_scales, m->sgu, c.H / 128, rows, c.H / 32, KC / 128,
                        moe::kFusedNeurons) &&
-         encode_u32_4d(&m->tm_dcodes, m->wd, kin_d, c.I / (4 * kin_d), c.H, c.E, RC) &&
+         encode_u32_4d(&m->tm_dcodes, m->wd, kin_d, IB / (4 * kin_d), c.H, c.E, RC) &&
          encode_u32_2d(&m->tm_dscales, m->sd, (uint64_t)c.H * c.I / 128, c.E,
                        (uint64_t)c.H * c.I / 32, RC * c.I / 128, 1);
 }
 
 cudaError_t set_fused_attributes(size_t smem) {
   cudaError_t e = cudaSuccess;
-  for (const void* f : {(const void*)moe::moe_layer_fused_t1<8>,
-                        (const void*)moe::moe_layer_fused_t1<32>})
+  for (const void* f : {(const void*)moe::moe_layer_fused_t1<8, moe::Mxfp8>,
+                        (const void*)moe::moe_layer_fused_t1<32, moe::Mxfp8>,
+                        (const void*)moe::moe_layer_fused_t1<8, moe::Mxfp4>,
+                        (const void*)moe::moe_layer_fused_t1<32, moe::Mxfp4>})
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   return e;
@@ -287,8 +320,12 @@ cudaError_t launch_fused(const moe_decode* m, const moe::FusedParams& fp, size_t
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = use_pdl(m) ? 2 : 1;
-  if (fp.k <= 8) return cudaLaunchKernelEx(&cfg, moe::moe_layer_fused_t1<8>, fp);
-  return cudaLaunchKernelEx(&cfg, moe::moe_layer_fused_t1<32>, fp);
+  if (is_fp4(m)) {
+    if (fp.k <= 8) return cudaLaunchKernelEx(&cfg, moe::moe_layer_fused_t1<8, moe::Mxfp4>, fp);
+    return cudaLaunchKernelEx(&cfg, moe::moe_layer_fused_t1<32, moe::Mxfp4>, fp);
+  }
+  if (fp.k <= 8) return cudaLaunchKernelEx(&cfg, moe::moe_layer_fused_t1<8, moe::Mxfp8>, fp);
+  return cudaLaunchKernelEx(&cfg, moe::moe_layer_fused_t1<32, moe::Mxfp8>, fp);
 }
 
 // Device limits shared by handles and the allocation-free call: SM count,
@@ -296,15 +333,25 @@ cudaError_t launch_fused(const moe_decode* m, const moe::FusedParams& fp, size_t
 // per SM (it then runs as a cooperative launch of num_sms CTAs).
 // The shared-memory limit of the gate/up kernels that stage x: the device's
 // opt-in maximum.
-cudaError_t set_xs_attributes(size_t smem) {
+template <class F>
+cudaError_t set_xs_attributes_f(size_t smem) {
   cudaError_t e = cudaSuccess;
-  for (const void* f : {(const void*)moe::moe_gate_up_3d_batched_xs<1, 8>, (const void*)moe::moe_gate_up_3d_batched_xs<2, 8>,
-                        (const void*)moe::moe_gate_up_3d_batched_xs<4, 8>, (const void*)moe::moe_gate_up_3d_batched_xs<8, 8>,
-                        (const void*)moe::moe_gate_up_3d_batched_xs<1, 32>, (const void*)moe::moe_gate_up_3d_batched_xs<2, 32>,
-                        (const void*)moe::moe_gate_up_3d_batched_xs<4, 32>, (const void*)moe::moe_gate_up_3d_batched_xs<8, 32>})
+  for (const void* f : {(const void*)moe::moe_gate_up_3d_batched_xs<1, 8, F>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<2, 8, F>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<4, 8, F>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<8, 8, F>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<1, 32, F>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<2, 32, F>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<4, 32, F>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<8, 32, F>})
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   return e;
+}
+
+cudaError_t set_xs_attributes(size_t smem) {
+  const cudaError_t e = set_xs_attributes_f<moe::Mxfp8>(smem);
+  return e == cudaSuccess ? set_xs_attributes_f<moe::Mxfp4>(smem) : e;
 }
 
 bool query_fused(moe_decode* m) {
@@ -325,8 +372,10 @@ bool query_fused(moe_decode* m) {
     return true;
   }
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, moe::moe_layer_fused_t1<8>,
-                                                    moe::kFusedThreads, smem) != cudaSuccess)
+  const void* fk = is_fp4(m) ? (const void*)moe::moe_layer_fused_t1<8, moe::Mxfp4>
+                             : (const void*)moe::moe_layer_fused_t1<8, moe::Mxfp8>;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fk, moe::kFusedThreads, smem) !=
+      cudaSuccess)
     return false;
   m->fused_ok = occ >= 1 && encode_fused_maps(m, fp.KC, fp.RC);
   return true;
@@ -437,7 +486,7 @@ moe_status_t moe_decode_create(const moe_decode_config_t* cfg, const uint8_t* w_
   if (c.E < 1 || c.k < 1 || c.H < 1 || c.I < 1 || c.max_T < 0) return MOE_ERR_INVALID_ARG;
   if (c.k > c.E) return MOE_ERR_INVALID_ARG;
   if (c.E > kMaxE || c.k > kMaxK || c.H % 32 || c.I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if ((c.flags & ~(MOE_FLAG_NO_PDL | MOE_FLAG_HOST_COPY)) != 0) return MOE_ERR_INVALID_ARG;
+  if ((c.flags & ~kKnownFlags) != 0) return MOE_ERR_INVALID_ARG;
   const size_t down_smem = (size_t)c.k * c.I * sizeof(float);
   if (down_smem > kMaxDownSmem) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(w_gateup, 32) || !aligned(w_down, 32)) return MOE_ERR_MISALIGNED;
@@ -462,13 +511,11 @@ moe_status_t moe_decode_create(const moe_decode_config_t* cfg, const uint8_t* w_
   ok = ok && query_fused(m);
 
 
-  // a per-function limit shared by every handle: always the library's maximum
-  ok = ok && cudaFuncSetAttribute(moe::moe_down_3d_batched<kDownQ>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kMaxDownSmem) == cudaSuccess;
+  ok = ok && set_down_attributes() == cudaSuccess;
   int occ = 0;
   ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                 &occ, moe::moe_gate_up_3d_batched<1, 8>, moe::kThreads, 0) == cudaSuccess;
+                 &occ, moe::moe_gate_up_3d_batched<1, 8, moe::Mxfp8>, moe::kThreads, 0) ==
+                 cudaSuccess;
   m->gate_up_ctas_per_sm = std::max(1, occ);
   if (ok && c.max_T > 0) {
     const size_t T = (size_t)c.max_T;
@@ -695,11 +742,9 @@ moe_status_t noalloc_device(int dev, NoAllocDevice* out) {
       return MOE_ERR_CUDA;
     int occ = 0;
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(moe::moe_down_3d_batched<kDownQ>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kMaxDownSmem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, moe::moe_gate_up_3d_batched<1, 8>,
-                                                      moe::kThreads, 0) != cudaSuccess)
+        set_down_attributes() != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &occ, moe::moe_gate_up_3d_batched<1, 8, moe::Mxfp8>, moe::kThreads, 0) != cudaSuccess)
       return MOE_ERR_CUDA;
     d.scratch = static_cast<uint8_t*>(ptr);
     d.gate_up_ctas_per_sm = std::max(1, occ);
@@ -728,7 +773,7 @@ extern "C" moe_status_t moe_decode_layer_noalloc(const moe_decode_config_t* cfg,
   if (c.E < 1 || c.k < 1 || c.H < 1 || c.I < 1 || T < 0) return MOE_ERR_INVALID_ARG;
   if (c.k > c.E) return MOE_ERR_INVALID_ARG;
   if (c.E > kMaxE || c.k > kMaxK || c.H % 32 || c.I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if ((c.flags & ~(MOE_FLAG_NO_PDL | MOE_FLAG_HOST_COPY)) != 0) return MOE_ERR_INVALID_ARG;
+  if ((c.flags & ~kKnownFlags) != 0) return MOE_ERR_INVALID_ARG;
   if ((size_t)c.k * c.I * sizeof(float) > kMaxDownSmem) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((size_t)T * c.k * c.I * 2 > kNoAllocHBytes) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(w_gateup, 32) || !aligned(w_down, 32)) return MOE_ERR_MISALIGNED;
@@ -760,9 +805,11 @@ extern "C" moe_status_t moe_decode_layer_noalloc(const moe_decode_config_t* cfg,
     size_t smem = 0;
     m.fused_ok = true;
     int occ = 0;
+    const void* fk = is_fp4(&m) ? (const void*)moe::moe_layer_fused_t1<8, moe::Mxfp4>
+                                : (const void*)moe::moe_layer_fused_t1<8, moe::Mxfp8>;
     m.fused_ok = plan_fused(&m, fp, smem) &&
-                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                     &occ, moe::moe_layer_fused_t1<8>, moe::kFusedThreads, smem) == cudaSuccess &&
+                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fk, moe::kFusedThreads,
+                                                               smem) == cudaSuccess &&
                  occ >= 1 && encode_fused_maps(&m, fp.KC, fp.RC);
   }
   return moe_decode_layer(&m, T, x, topk_ids, topk_w, reinterpret_cast<uint16_t*>(d.scratch), y,

@@ -35,6 +35,15 @@ __device__ __forceinline__ uint4 ld_act16(const void* p) {
   return v;
 }
 
+// 16 bytes of a weight row read once per step (the 32 codes of one MXFP4
+// block): no L1 allocation (the L2 eviction-priority form of the load exists
+// for 256-bit accesses only).
+__device__ __forceinline__ void ld_weights16(const uint8_t* p, uint32_t (&r)[4]) {
+  asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "l"(p));
+}
+
 __device__ __forceinline__ uint32_t ld_scale(const uint8_t* p) {
   unsigned short v;
   asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));

@@ -1,13 +1,15 @@
 // f16 block arithmetic shared by the kernels: activations (x, h) held in
 // shared memory as 32-element blocks of f16, each block multiplied by the
 // power of two 2^e that brings its largest magnitude into [2^14, 2^15) (the
-// factor 2^-e is applied to the block's dot product), and E4M3 weight codes
-// converted to f16 with cvt.rn.f16x2.e4m3x2.
+// factor 2^-e is applied to the block's dot product), and weight codes
+// converted to f16 with cvt.rn.f16x2.e4m3x2 (MXFP8) or cvt.rn.f16x2.e2m1x2
+// (MXFP4). The two weight formats are the types Mxfp8 and Mxfp4 at the end,
+// which every kernel takes as a template argument.
 //
-// Exactness: E4M3 -> f16 is exact, a bf16 value scaled that way is exact in
-// f16 whenever it lies within 2^-28 of its block's largest magnitude, and an
-// f16 x f16 product is exact in FP32, so fma.rn.f32.f16 gives the same sums
-// as FP32 FMAs on the decoded values.
+// Exactness: E4M3 -> f16 and E2M1 -> f16 are exact, a bf16 value scaled that
+// way is exact in f16 whenever it lies within 2^-28 of its block's largest
+// magnitude, and an f16 x f16 product is exact in FP32, so fma.rn.f32.f16
+// gives the same sums as FP32 FMAs on the decoded values.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -167,5 +169,100 @@ __device__ __forceinline__ float dot_block_h(const uint32_t (&wh)[16], const uin
   fma_f16x4(r, s, wh[14], wh[15], x3.z, x3.w);
   return (p + q) + (r + s);
 }
+
+// ---------------------------------------------------------------------------
+// MXFP4 elements: E2M1 codes, two to a byte, element 2c in the low nibble of
+// byte c (the element format the GC-MoE summary, onedev.kr/papers/1690, "How
+// it is used", gives its routed weights; the packing follows the OCP MX
+// convention). cvt.rn.f16x2.e2m1x2 turns one byte into an f16 pair, its low
+// nibble into the low half.
+// ---------------------------------------------------------------------------
+
+// Eight E2M1 codes (one word, nibble n = element n) -> four f16x2 words:
+// elements 0,1 / 2,3 / 4,5 / 6,7.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t codes, uint32_t& w01, uint32_t& w23,
+                                                uint32_t& w45, uint32_t& w67) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(w01), "=r"(w23), "=r"(w45), "=r"(w67)
+      : "r"(codes));
+}
+
+// f16x2 word -> two FP32 values (exact).
+__device__ __forceinline__ void f16x2_to_f32(uint32_t w, float& lo, float& hi) {
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w));
+}
+
+// ---------------------------------------------------------------------------
+// The weight formats. Each describes one 32-element block of a weight row:
+//   kBlockBytes    code bytes of the block (rows are K * kBlockBytes / 32 bytes)
+//   kWords         32-bit words holding them
+//   load(p, q)     the block's codes from global memory (streamed, see ld_weights32)
+//   decode(q, swap, wh)  16 f16x2 words: elements 0..15 then 16..31, or the
+//                  two halves the other way round when `swap` (the order in
+//                  which LaneBlock pairs them with activation chunks)
+//   chunk_f32(q, c, v)   elements 8c .. 8c+7 as FP32
+//   dot_smem(codes, act, lb)  the block's dot with an f16 activation block,
+//                  codes read from shared memory
+// ---------------------------------------------------------------------------
+
+struct Mxfp8 {
+  static constexpr int kBlockBytes = 32;
+  static constexpr int kWords = 8;
+  __device__ __forceinline__ static void load(const uint8_t* p, uint32_t (&q)[kWords]) {
+    ld_weights32(p, q);
+  }
+  __device__ __forceinline__ static void decode(const uint32_t (&q)[kWords], bool swap,
+                                                uint32_t (&wh)[16]) {
+    decode_block_f16(q, swap, wh);
+  }
+  __device__ __forceinline__ static void chunk_f32(const uint32_t (&q)[kWords], int c,
+                                                   float (&v)[8]) {
+    e4m3x4_to_f32(q[2 * c], v[0], v[1], v[2], v[3]);
+    e4m3x4_to_f32(q[2 * c + 1], v[4], v[5], v[6], v[7]);
+  }
+  __device__ __forceinline__ static float dot_smem(const uint8_t* codes, const uint8_t* act,
+                                                   const LaneBlock& lb) {
+    return dot_block(codes, act, lb);
+  }
+};
+
+struct Mxfp4 {
+  static constexpr int kBlockBytes = 16;
+  static constexpr int kWords = 4;
+  __device__ __forceinline__ static void load(const uint8_t* p, uint32_t (&q)[kWords]) {
+    ld_weights16(p, q);
+  }
+  __device__ __forceinline__ static void decode(const uint32_t (&q)[kWords], bool swap,
+                                                uint32_t (&wh)[16]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t v = swap ? q[c ^ 2] : q[c];
+      e2m1x8_to_f16x2(v, wh[4 * c], wh[4 * c + 1], wh[4 * c + 2], wh[4 * c + 3]);
+    }
+  }
+  __device__ __forceinline__ static void chunk_f32(const uint32_t (&q)[kWords], int c,
+                                                   float (&v)[8]) {
+    uint32_t w[4];
+    e2m1x8_to_f16x2(q[c], w[0], w[1], w[2], w[3]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f16x2_to_f32(w[i], v[2 * i], v[2 * i + 1]);
+  }
+  // A warp's 32 lanes read 32 consecutive 16-byte blocks: conflict-free
+  // without the half swap MXFP8's 32-byte blocks need, so the codes are
+  // reordered in registers instead.
+  __device__ __forceinline__ static float dot_smem(const uint8_t* codes, const uint8_t* act,
+                                                   const LaneBlock& lb) {
+    const uint4 a = *reinterpret_cast<const uint4*>(codes);
+    const uint32_t q[4] = {a.x, a.y, a.z, a.w};
+    uint32_t wh[16];
+    decode(q, lb.c_first != 0, wh);
+    return dot_block_h(wh, act, lb);
+  }
+};
 
 }  // namespace moe

@@ -2,9 +2,12 @@
 //
 // Output-centric throughout (the warp-decode post, cursor.com/blog/warp-decode,
 // "What we changed" and "How the two kernels work"): every warp owns output
-// scalars, streams the weight rows they need straight from HBM, decodes MXFP8
-// to FP32 in registers, accumulates in private registers and finishes with a
-// shfl.xor butterfly. No warp shares partial sums with another.
+// scalars, streams the weight rows they need straight from HBM, decodes the
+// block-scaled codes in registers, accumulates in private FP32 registers and
+// finishes with a shfl.xor butterfly. No warp shares partial sums with
+// another. The projection kernels take the weight format (Mxfp8 or Mxfp4) as
+// a template argument F; a weight row of K elements is K * F::kBlockBytes / 32
+// code bytes.
 #pragma once
 
 #include "moe_f16blocks.cuh"
@@ -132,16 +135,17 @@ __global__ void __launch_bounds__(32) moe_dedup_schedule_kernel(const int32_t* _
 struct GateUpParams {
   const uint16_t* x;      // [T, H] bf16
   const int32_t* ids;     // [T, k]
-  const uint8_t* wgu;     // [E, 2I, H]
+  const uint8_t* wgu;     // [E, 2I, H * F::kBlockBytes / 32]
   const uint8_t* sgu;     // [E, 2I, H/32]
   uint16_t* h;            // [T, k, I] bf16
   uint32_t* err;
   int T, k, E, H, I;
 };
 
-template <int NT>
-__device__ __forceinline__ void gate_up_block(const uint32_t (&qg)[8], const uint32_t (&qu)[8],
-                                              float scg, float scu, const uint16_t* __restrict__ x,
+template <int NT, class F>
+__device__ __forceinline__ void gate_up_block(const uint32_t (&qg)[F::kWords],
+                                              const uint32_t (&qu)[F::kWords], float scg,
+                                              float scu, const uint16_t* __restrict__ x,
                                               const int (&tok)[NT], int nt, int H, int b,
                                               float (&ag)[NT], float (&au)[NT]) {
   float pg[NT], pu[NT];
@@ -150,10 +154,8 @@ __device__ __forceinline__ void gate_up_block(const uint32_t (&qg)[8], const uin
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     float g[8], u[8];
-    e4m3x4_to_f32(qg[2 * c], g[0], g[1], g[2], g[3]);
-    e4m3x4_to_f32(qg[2 * c + 1], g[4], g[5], g[6], g[7]);
-    e4m3x4_to_f32(qu[2 * c], u[0], u[1], u[2], u[3]);
-    e4m3x4_to_f32(qu[2 * c + 1], u[4], u[5], u[6], u[7]);
+    F::chunk_f32(qg, c, g);
+    F::chunk_f32(qu, c, u);
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
       if (n < nt) {
@@ -175,7 +177,7 @@ __device__ __forceinline__ void gate_up_block(const uint32_t (&qg)[8], const uin
   }
 }
 
-template <int NT, int KMAX>
+template <int NT, int KMAX, class F>
 __global__ void __launch_bounds__(kThreads, 2) moe_gate_up_3d_batched(GateUpParams p) {
   __shared__ uint32_t sm_words[kWarps][32];
   const int lane = threadIdx.x & 31;
@@ -203,9 +205,11 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gate_up_3d_batched(GateUpPara
     const int e = s.expert(u);
     const uint32_t jm = s.jmask(e);
     uint32_t tokens = __ballot_sync(kFull, jm != 0u);
+    constexpr int CB = F::kBlockBytes;
+    const size_t RB = (size_t)nb * CB;        // code bytes per row
     const size_t row = (size_t)e * 2 * I + i;
-    const uint8_t* wg = p.wgu + row * H;
-    const uint8_t* wu = wg + (size_t)I * H;
+    const uint8_t* wg = p.wgu + row * RB;
+    const uint8_t* wu = wg + (size_t)I * RB;
     const uint8_t* sg = p.sgu + row * nb;
     const uint8_t* su = sg + (size_t)I * nb;
     while (tokens) {
@@ -223,35 +227,35 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gate_up_3d_batched(GateUpPara
 #pragma unroll
       for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
       // two blocks in flight per lane: issue block b+32 before computing b
-      uint32_t qg0[8], qu0[8], qg1[8], qu1[8];
+      uint32_t qg0[F::kWords], qu0[F::kWords], qg1[F::kWords], qu1[F::kWords];
       uint32_t s0g = 0, s0u = 0, s1g = 0, s1u = 0;
       int b = lane;
       if (b < nb) {
-        ld_weights32(wg + b * 32, qg0);
-        ld_weights32(wu + b * 32, qu0);
+        F::load(wg + b * CB, qg0);
+        F::load(wu + b * CB, qu0);
         s0g = ld_scale(sg + b);
         s0u = ld_scale(su + b);
       }
       while (b < nb) {
         const int b1 = b + 32;
         if (b1 < nb) {
-          ld_weights32(wg + b1 * 32, qg1);
-          ld_weights32(wu + b1 * 32, qu1);
+          F::load(wg + b1 * CB, qg1);
+          F::load(wu + b1 * CB, qu1);
           s1g = ld_scale(sg + b1);
           s1u = ld_scale(su + b1);
         }
-        gate_up_block<NT>(qg0, qu0, ue8m0_to_f32(s0g), ue8m0_to_f32(s0u), p.x, tok, nt, H, b, ag,
-                          au);
+        gate_up_block<NT, F>(qg0, qu0, ue8m0_to_f32(s0g), ue8m0_to_f32(s0u), p.x, tok, nt, H, b,
+                             ag, au);
         if (b1 >= nb) break;
         const int b2 = b1 + 32;
         if (b2 < nb) {
-          ld_weights32(wg + b2 * 32, qg0);
-          ld_weights32(wu + b2 * 32, qu0);
+          F::load(wg + b2 * CB, qg0);
+          F::load(wu + b2 * CB, qu0);
           s0g = ld_scale(sg + b2);
           s0u = ld_scale(su + b2);
         }
-        gate_up_block<NT>(qg1, qu1, ue8m0_to_f32(s1g), ue8m0_to_f32(s1u), p.x, tok, nt, H, b1, ag,
-                          au);
+        gate_up_block<NT, F>(qg1, qu1, ue8m0_to_f32(s1g), ue8m0_to_f32(s1u), p.x, tok, nt, H, b1,
+                             ag, au);
         b = b2;
       }
 #pragma unroll
@@ -286,7 +290,7 @@ struct DownParams {
   const uint16_t* h;      // [T, k, I] bf16
   const int32_t* ids;     // [T, k]
   const float* w;         // [T, k]
-  const uint8_t* wd;      // [E, H, I]
+  const uint8_t* wd;      // [E, H, I * F::kBlockBytes / 32]
   const uint8_t* sd;      // [E, H, I/32]
   uint16_t* y;            // [T, H] bf16
   uint32_t* err;
@@ -294,9 +298,9 @@ struct DownParams {
   int early;
 };
 
-template <int QMAX>
+template <int QMAX, class F>
 __device__ __forceinline__ void down_load_round(const DownParams& p, int f0, int nf, int nbI, int r,
-                                                int id, float wj, uint32_t (&q)[QMAX][8],
+                                                int id, float wj, uint32_t (&q)[QMAX][F::kWords],
                                                 float (&sc)[QMAX], float (&wsel)[QMAX],
                                                 bool (&valid)[QMAX]) {
   const int lane = threadIdx.x & 31;
@@ -310,11 +314,11 @@ __device__ __forceinline__ void down_load_round(const DownParams& p, int f0, int
     valid[qi] = (f < nf) && (e >= 0);
     if (valid[qi]) {
       const size_t rowi = (size_t)e * p.H + r;
-      ld_weights32(p.wd + rowi * p.I + b * 32, q[qi]);
+      F::load(p.wd + (rowi * nbI + b) * F::kBlockBytes, q[qi]);
       sc[qi] = ue8m0_to_f32(ld_scale(p.sd + rowi * nbI + b));
     } else {
 #pragma unroll
-      for (int m = 0; m < 8; ++m) q[qi][m] = 0u;
+      for (int m = 0; m < F::kWords; ++m) q[qi][m] = 0u;
       sc[qi] = 0.f;
     }
   }
@@ -338,7 +342,7 @@ __host__ __device__ constexpr size_t gate_up_xs_smem(int T, int H) {
   return (size_t)kXsWarps * 32 * 4 + (size_t)T * (H >> 5) * (64 + 4);
 }
 
-template <int NT, int KMAX>
+template <int NT, int KMAX, class F>
 __global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_3d_batched_xs(GateUpParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
@@ -382,9 +386,11 @@ __global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_3d_batched_xs(GateU
     const int e = s.expert(u);
     const uint32_t jm = s.jmask(e);
     uint32_t tokens = __ballot_sync(kFull, jm != 0u);
+    constexpr int CB = F::kBlockBytes;
+    const size_t RB = (size_t)nb * CB;        // code bytes per row
     const size_t row = (size_t)e * 2 * I + i;
-    const uint8_t* wg = p.wgu + row * H;
-    const uint8_t* wu = wg + (size_t)I * H;
+    const uint8_t* wg = p.wgu + row * RB;
+    const uint8_t* wu = wg + (size_t)I * RB;
     const uint8_t* sg = p.sgu + row * nb;
     const uint8_t* su = sg + (size_t)I * nb;
 #pragma unroll 1
@@ -403,24 +409,24 @@ __global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_3d_batched_xs(GateU
 #pragma unroll
       for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
       // the next block's codes are in flight while this one is applied
-      uint32_t qg[8], qu[8];
+      uint32_t qg[F::kWords], qu[F::kWords];
       uint32_t s_g = 0, s_u = 0;
       int b = lane;
       if (b < nb) {
-        ld_weights32(wg + b * 32, qg);
-        ld_weights32(wu + b * 32, qu);
+        F::load(wg + b * CB, qg);
+        F::load(wu + b * CB, qu);
         s_g = ld_scale(sg + b);
         s_u = ld_scale(su + b);
       }
 #pragma unroll 1
       for (; b < nb; b += 32) {
         uint32_t whg[16], whu[16];
-        decode_block_f16(qg, swap, whg);
-        decode_block_f16(qu, swap, whu);
+        F::decode(qg, swap, whg);
+        F::decode(qu, swap, whu);
         const float scg = ue8m0_to_f32(s_g), scu = ue8m0_to_f32(s_u);
         if (b + 32 < nb) {
-          ld_weights32(wg + (b + 32) * 32, qg);
-          ld_weights32(wu + (b + 32) * 32, qu);
+          F::load(wg + (b + 32) * CB, qg);
+          F::load(wu + (b + 32) * CB, qu);
           s_g = ld_scale(sg + b + 32);
           s_u = ld_scale(su + b + 32);
         }
@@ -462,9 +468,9 @@ __host__ __device__ constexpr size_t down_xs_smem(int k, int I) {
   return (size_t)k * (I >> 5) * (64 + 4);
 }
 
-template <int QMAX>
+template <int QMAX, class F>
 __device__ __forceinline__ float down_compute_round_xs(const uint8_t* hs, const float* hfac, int f0,
-                                                       const uint32_t (&q)[QMAX][8],
+                                                       const uint32_t (&q)[QMAX][F::kWords],
                                                        const float (&sc)[QMAX],
                                                        const float (&wsel)[QMAX],
                                                        const bool (&valid)[QMAX],
@@ -475,7 +481,7 @@ __device__ __forceinline__ float down_compute_round_xs(const uint8_t* hs, const 
     if (valid[qi]) {
       const int f = f0 + lane + 32 * qi;
       uint32_t wh[16];
-      decode_block_f16(q[qi], swap, wh);
+      F::decode(q[qi], swap, wh);
       const float d = dot_block_h(wh, hs + 64 * f, lb);
       acc = fmaf(d * hfac[f] * sc[qi], wsel[qi], acc);
     }
@@ -483,7 +489,7 @@ __device__ __forceinline__ float down_compute_round_xs(const uint8_t* hs, const 
   return acc;
 }
 
-template <int QMAX>
+template <int QMAX, class F>
 __global__ void __launch_bounds__(kThreads, 2) moe_down_3d_batched(DownParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
@@ -504,10 +510,10 @@ __global__ void __launch_bounds__(kThreads, 2) moe_down_3d_batched(DownParams p)
       id = -1;
     }
   }
-  uint32_t q[QMAX][8];
+  uint32_t q[QMAX][F::kWords];
   float sc[QMAX], wsel[QMAX];
   bool valid[QMAX];
-  down_load_round<QMAX>(p, 0, nf, nbI, r, id, wj, q, sc, wsel, valid);
+  down_load_round<QMAX, F>(p, 0, nf, nbI, r, id, wj, q, sc, wsel, valid);
   if (p.early) pdl_wait();   // h is written by the gate/up kernel
   {
     const uint4* ht = reinterpret_cast<const uint4*>(p.h + (size_t)t * k * I);
@@ -522,10 +528,10 @@ __global__ void __launch_bounds__(kThreads, 2) moe_down_3d_batched(DownParams p)
   pdl_trigger();
   const LaneBlock lb(lane);
   const bool swap = lb.c_first != 0;
-  float acc = down_compute_round_xs<QMAX>(hs, hfac, 0, q, sc, wsel, valid, lb, swap, 0.f);
+  float acc = down_compute_round_xs<QMAX, F>(hs, hfac, 0, q, sc, wsel, valid, lb, swap, 0.f);
   for (int f0 = 32 * QMAX; f0 < nf; f0 += 32 * QMAX) {
-    down_load_round<QMAX>(p, f0, nf, nbI, r, id, wj, q, sc, wsel, valid);
-    acc = down_compute_round_xs<QMAX>(hs, hfac, f0, q, sc, wsel, valid, lb, swap, acc);
+    down_load_round<QMAX, F>(p, f0, nf, nbI, r, id, wj, q, sc, wsel, valid);
+    acc = down_compute_round_xs<QMAX, F>(hs, hfac, f0, q, sc, wsel, valid, lb, swap, acc);
   }
   acc = warp_sum(acc);
   if (lane == 0) p.y[(size_t)t * p.H + r] = f32_to_bf16_rn(acc);

@@ -25,15 +25,17 @@
 // slower on this part: every CTA polling all of h floods L2 while the down
 // rows stream.)
 //
-// Arithmetic. Each lane reduces one 32-element MX block at a time: 32 E4M3
-// codes against 32 activations, FP32 accumulation, then the block's UE8M0
-// scale. The activations (x in the gate/up phase, h in the down phase) are
-// held in shared memory as f16 after multiplying each 32-element block by a
-// power of two 2^e that brings its largest magnitude into [2^14, 2^15); the
-// factor 2^-e is applied to the block's sum. E4M3 -> f16 is exact, a bf16
-// value scaled that way is exact in f16 whenever it lies within 2^-28 of its
-// block's largest magnitude, and an f16 x f16 product is exact in FP32, so
-// fma.rn.f32.f16 gives the same sums as FP32 FMAs on the decoded values.
+// Arithmetic. Each lane reduces one 32-element MX block at a time: 32 codes
+// (E4M3 for MXFP8, E2M1 for MXFP4: the template argument F) against 32
+// activations, FP32 accumulation, then the block's UE8M0 scale. The
+// activations (x in the gate/up phase, h in the down phase) are held in
+// shared memory as f16 after multiplying each 32-element block by a power of
+// two 2^e that brings its largest magnitude into [2^14, 2^15); the factor
+// 2^-e is applied to the block's sum. Both code types convert to f16
+// exactly, a bf16 value scaled that way is exact in f16 whenever it lies
+// within 2^-28 of its block's largest magnitude, and an f16 x f16 product is
+// exact in FP32, so fma.rn.f32.f16 gives the same sums as FP32 FMAs on the
+// decoded values.
 #pragma once
 
 #include <cuda.h>
@@ -49,23 +51,26 @@ constexpr int kFusedConsumers = 15;                       // consumer warps
 constexpr int kFusedThreads = (kFusedConsumers + 1) * 32; // + one producer warp
 constexpr int kFusedNeurons = kFusedConsumers;            // gate/up neurons per stage
 
+// Byte counts below: a row of K weights holds K * F::kBlockBytes / 32 code
+// bytes (RB for a gate/up row of H, IB for a down row of I, KB for a K-chunk
+// of KC).
 struct FusedParams {
-  // W_gateup codes as a 3D uint32 tensor [E*2I][H/(4*kin)][kin] with boxes of
-  // kFusedNeurons rows x KC codes, and its scales as a 2D uint32 tensor
+  // W_gateup codes as a 3D uint32 tensor [E*2I][RB/(4*kin)][kin] with boxes of
+  // kFusedNeurons rows x KB bytes, and its scales as a 2D uint32 tensor
   // [E*2I][H/128] with boxes of kFusedNeurons rows x KC/32 scale bytes
   CUtensorMap tm_codes;
   CUtensorMap tm_scales;
-  // W_down codes as a 4D uint32 tensor [E][H][I/(4*kin_d)][kin_d] with boxes of
-  // RC rows of one expert, and its scales as a 2D uint32 tensor [E][H*I/128]
-  // with boxes of RC rows' scale bytes (rows past H read as zeros)
+  // W_down codes as a 4D uint32 tensor [E][H][IB/(4*kin_d)][kin_d] with boxes
+  // of RC rows of one expert, and its scales as a 2D uint32 tensor
+  // [E][H*I/128] with boxes of RC rows' scale bytes (rows past H read as zeros)
   CUtensorMap tm_dcodes;
   CUtensorMap tm_dscales;
   const uint16_t* x;          // [1, H] bf16
   const int32_t* ids;         // [1, k]
   const float* w;             // [1, k]
-  const uint8_t* wgu;         // [E, 2I, H]
+  const uint8_t* wgu;         // [E, 2I, RB]
   const uint8_t* sgu;         // [E, 2I, H/32]
-  const uint8_t* wd;          // [E, H, I]
+  const uint8_t* wd;          // [E, H, IB]
   const uint8_t* sd;          // [E, H, I/32]
   uint16_t* h;                // [1, k, I] bf16 (written, then read back through L2)
   uint16_t* y;                // [1, H] bf16
@@ -73,31 +78,32 @@ struct FusedParams {
   unsigned long long* launch_ctr;  // grows by gridDim.x per launch, at kernel start
   unsigned long long* bar_ctr;     // grows by gridDim.x per launch, at the grid barrier
   int k, E, H, I;
-  int KC;       // gate/up codes per row per stage: 512, 1024 or 2048, divides H
-  int kin;      // uint32 words per innermost box row of tm_codes (KC/4 or 256)
+  int KC;       // gate/up weights per row per stage (KB = 512, 1024 or 2048 bytes), divides H
+  int kin;      // uint32 words per innermost box row of tm_codes (KB/4 or 256)
   int SG;       // gate/up ring slots
-  int slot_g;   // bytes per gate/up slot (GuStageLayout(KC).end)
+  int slot_g;   // bytes per gate/up slot (GuStageLayout(KB, KC).end)
   int SR;       // down row chunks per ring slot (one routed expert's RC rows each)
   int slot_d;   // bytes per down chunk in a slot: RC rows of codes, then RC rows of scales
   int RG;       // down row granule (keeps scale copies 16-byte aligned)
   int RC;       // down rows per chunk (multiple of RG, <= kFusedConsumers)
   int nkc;      // H / KC: K-chunks per gate/up row
-  int kdiv;     // KC / (4 * kin): tm_codes dim-1 boxes per K-chunk
+  int kdiv;     // KB / (4 * kin): tm_codes dim-1 boxes per K-chunk
   int nrg;      // H / RG: down row granules
 };
 
 __host__ __device__ constexpr int round128(int v) { return (v + 127) / 128 * 128; }
 
-// Byte offsets of a gate/up stage in a ring slot: gate codes, up codes, gate
-// scales, up scales, each region starting on a 128-byte boundary (the TMA
-// tensor copies that fill them require it); `end` is the bytes used.
+// Byte offsets of a gate/up stage (KB code bytes and KC/32 scale bytes per
+// row) in a ring slot: gate codes, up codes, gate scales, up scales, each
+// region starting on a 128-byte boundary (the TMA tensor copies that fill
+// them require it); `end` is the bytes used.
 struct GuStageLayout {
   int up, gs, us, end;
-  __host__ __device__ explicit GuStageLayout(int KC)
-      : up(round128(kFusedNeurons * KC)),
-        gs(2 * round128(kFusedNeurons * KC)),
-        us(2 * round128(kFusedNeurons * KC) + round128(kFusedNeurons * (KC >> 5))),
-        end(2 * round128(kFusedNeurons * KC) + 2 * round128(kFusedNeurons * (KC >> 5))) {}
+  __host__ __device__ GuStageLayout(int KB, int KC)
+      : up(round128(kFusedNeurons * KB)),
+        gs(2 * round128(kFusedNeurons * KB)),
+        us(2 * round128(kFusedNeurons * KB) + round128(kFusedNeurons * (KC >> 5))),
+        end(2 * round128(kFusedNeurons * KB) + 2 * round128(kFusedNeurons * (KC >> 5))) {}
 };
 
 // Shared-memory map of the kernel (byte offsets, each 128-byte aligned). The
@@ -278,10 +284,12 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* bar, unsigne
   return false;
 }
 
-template <int KMAX>
+template <int KMAX, class F>
 __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int CB = F::kBlockBytes;
   const int H = p.H, I = p.I, KC = p.KC, SG = p.SG, nbI = I >> 5;
+  const int KB = (KC >> 5) * CB, IB = nbI * CB;   // code bytes of a K-chunk, of a down row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const FusedSmem L(SG, p.slot_g, H, I, p.k);
   uint8_t* ring_g = smem;
@@ -339,7 +347,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   dw.rows(p);
   s.finish(p.E, sm_words + warp * 32, p.err);
   const int nU = s.n_unique;
-  const GuStageLayout lay(KC);
+  const GuStageLayout lay(KB, KC);
 
   if (warp == kFusedConsumers) {
     // ------------------------------------------------------------ producer
@@ -363,7 +371,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
         if (lane == 0) {
           // four tensor copies: the stage's gate rows, up rows, and their
           // scales (full boxes; rows past the expert are never read)
-          mbar_expect_tx(bar, 2u * kFusedNeurons * KC + 2u * kFusedNeurons * (KC >> 5));
+          mbar_expect_tx(bar, 2u * kFusedNeurons * KB + 2u * kFusedNeurons * (KC >> 5));
           const int row = e * 2 * I + gw.i0;
           const int kchunk = gw.kc * p.kdiv;
           tma_load_3d(dst, &p.tm_codes, 0, kchunk, row, bar);
@@ -376,14 +384,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
         // a down group: two tensor copies per expert, RC rows of codes and
         // their scales (full boxes: rows of the next chunk, or zeros past H,
         // are never read)
-        if (lane == 0) mbar_expect_tx(bar, (uint32_t)p.RC * (I + nbI) * dw.ng);
+        if (lane == 0) mbar_expect_tx(bar, (uint32_t)p.RC * (IB + nbI) * dw.ng);
         #pragma unroll 1
         for (int ui = 0; ui < dw.ng; ++ui) {
           const int e = s.expert(dw.u0 + ui);   // warp-collective
           if (lane == 0) {
             uint8_t* d = dst + (size_t)ui * p.slot_d;
             tma_load_4d(d, &p.tm_dcodes, 0, 0, dw.c0, e, bar);
-            tma_load_2d(d + (size_t)p.RC * I, &p.tm_dscales, dw.c0 * (nbI >> 2), e, bar);
+            tma_load_2d(d + (size_t)p.RC * IB, &p.tm_dscales, dw.c0 * (nbI >> 2), e, bar);
           }
         }
         dw.next();
@@ -456,8 +464,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
           const int b = gw.kc * nbk + bl;         // block of the H row
           const uint8_t* act = xs + 64 * b;
           const float fx = xf[b];
-          const float dg = dot_block(base + warp * KC + 32 * bl, act, lb);
-          const float du = dot_block(base + lay.up + warp * KC + 32 * bl, act, lb);
+          const float dg = F::dot_smem(base + warp * KB + CB * bl, act, lb);
+          const float du = F::dot_smem(base + lay.up + warp * KB + CB * bl, act, lb);
           ag = fmaf(dg * fx, ue8m0_to_f32(base[lay.gs + warp * nbk + bl]), ag);
           au = fmaf(du * fx, ue8m0_to_f32(base[lay.us + warp * nbk + bl]), au);
         }
@@ -503,8 +511,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
       const int g = u / p.SR;
       const int slot = pos0.slot + g < SG ? pos0.slot + g : pos0.slot + g - SG;
       const int off = slot * p.slot_g + (u - g * p.SR) * p.slot_d;
-      tc[t] = off + 32 * b;
-      ts[t] = off + p.RC * I + b;
+      tc[t] = off + CB * b;
+      ts[t] = off + p.RC * IB + b;
     }
   };
   // ... and the arrival of its groups
@@ -546,7 +554,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   }
   named_sync(1, ncons);   // h staged
   {
-    const int wI = warp * I, wS = warp * nbI;
+    const int wI = warp * IB, wS = warp * nbI;
     #pragma unroll 1
     while (have) {
       float acc = 0.f;
@@ -556,8 +564,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
           // this item and the one 32 further on (the same one again past the end)
           const bool two = t + 32 < n_items;
           const int t2 = two ? t + 32 : t;
-          const float d1 = dot_block(smem + tc[t] + wI, hs + 64 * t, lb);
-          const float d2 = dot_block(smem + tc[t2] + wI, hs + 64 * t2, lb);
+          const float d1 = F::dot_smem(smem + tc[t] + wI, hs + 64 * t, lb);
+          const float d2 = F::dot_smem(smem + tc[t2] + wI, hs + 64 * t2, lb);
           acc = fmaf(d1 * ue8m0_to_f32(smem[ts[t] + wS]), tf[t], acc);
           if (two) acc = fmaf(d2 * ue8m0_to_f32(smem[ts[t2] + wS]), tf[t2], acc);
         }

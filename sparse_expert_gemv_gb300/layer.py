@@ -9,7 +9,7 @@ import ctypes
 
 import torch
 
-from ._lib import MoEConfig, check, lib
+from ._lib import MOE_FLAG_MXFP4, MoEConfig, check, lib
 
 
 def _ptr(t: torch.Tensor | None) -> int:
@@ -49,23 +49,31 @@ def _need(t: torch.Tensor, dtype: torch.dtype, shape: tuple, name: str, cuda: bo
 
 
 class MoEDecode:
-    """One MoE decode layer over caller-owned MXFP8 weights on the current device.
+    """One MoE decode layer over caller-owned block-scaled weights on the current device.
 
-    w_gateup uint8 [E, 2I, H] (rows [0, I) gate, [I, 2I) up), s_gateup uint8
-    [E, 2I, H/32], w_down uint8 [E, H, I], s_down uint8 [E, H, I/32]. The
+    fmt="mxfp8": w_gateup uint8 [E, 2I, H] (rows [0, I) gate, [I, 2I) up),
+    w_down uint8 [E, H, I], one E4M3 code per byte. fmt="mxfp4": w_gateup
+    uint8 [E, 2I, H/2], w_down uint8 [E, H, I/2], two E2M1 codes per byte
+    (the even element in the low nibble). Either way s_gateup uint8
+    [E, 2I, H/32] and s_down uint8 [E, H, I/32] hold the UE8M0 scales. The
     tensors are borrowed (kept alive by this object, never copied).
     """
 
     def __init__(self, w_gateup, s_gateup, w_down, s_down, *, k: int, max_T: int = 32,
-                 flags: int = 0):
-        E, twoI, H = w_gateup.shape
-        I = twoI // 2
-        _need(w_gateup, torch.uint8, (E, 2 * I, H), "w_gateup")
+                 flags: int = 0, fmt: str = "mxfp8"):
+        if fmt not in ("mxfp8", "mxfp4"):
+            raise ValueError(f"fmt must be 'mxfp8' or 'mxfp4', got {fmt!r}")
+        per = 2 if fmt == "mxfp4" else 1          # elements per code byte
+        E, twoI, RB = w_gateup.shape
+        I, H = twoI // 2, RB * per
+        _need(w_gateup, torch.uint8, (E, 2 * I, H // per), "w_gateup")
         _need(s_gateup, torch.uint8, (E, 2 * I, H // 32), "s_gateup")
-        _need(w_down, torch.uint8, (E, H, I), "w_down")
+        _need(w_down, torch.uint8, (E, H, I // per), "w_down")
         _need(s_down, torch.uint8, (E, H, I // 32), "s_down")
-        self.E, self.k, self.H, self.I, self.max_T = E, k, H, I, max_T
+        self.E, self.k, self.H, self.I, self.max_T, self.fmt = E, k, H, I, max_T, fmt
         self._weights = (w_gateup, s_gateup, w_down, s_down)
+        if fmt == "mxfp4":
+            flags |= MOE_FLAG_MXFP4
         cfg = MoEConfig(E, k, H, I, max_T, flags)
         h = ctypes.c_void_p()
         check(lib.moe_decode_create(ctypes.byref(cfg), _ptr(w_gateup), _ptr(s_gateup),

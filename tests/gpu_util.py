@@ -16,14 +16,19 @@ def tensor_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def device_weights(w: wl.Workload, experts: dict, device, fill_code=wl.NAN_CODE):
+def device_weights(w: wl.Workload, experts: dict, device, fill_code=wl.NAN_CODE, fmt="mxfp8"):
     """Full [E, ...] device tensors; experts absent from `experts` hold NaN codes
-    (a kernel that reads them poisons exactly the outputs that used them)."""
+    (MXFP8) or NaN scales (MXFP4, whose codes have no NaN), so a kernel that
+    reads them poisons exactly the outputs that used them."""
     E, H, I = w.E, w.H, w.I
-    wgu = torch.full((E, 2 * I, H), fill_code, dtype=torch.uint8, device=device)
-    sgu = torch.full((E, 2 * I, H // 32), 127, dtype=torch.uint8, device=device)
-    wd = torch.full((E, H, I), fill_code, dtype=torch.uint8, device=device)
-    sd = torch.full((E, H, I // 32), 127, dtype=torch.uint8, device=device)
+    per = 2 if fmt == "mxfp4" else 1
+    fill_scale = 127
+    if fmt == "mxfp4":
+        fill_code, fill_scale = 0x77, 0xFF
+    wgu = torch.full((E, 2 * I, H // per), fill_code, dtype=torch.uint8, device=device)
+    sgu = torch.full((E, 2 * I, H // 32), fill_scale, dtype=torch.uint8, device=device)
+    wd = torch.full((E, H, I // per), fill_code, dtype=torch.uint8, device=device)
+    sd = torch.full((E, H, I // 32), fill_scale, dtype=torch.uint8, device=device)
     for e, (a, b, c, d) in experts.items():
         wgu[e].copy_(torch.from_numpy(a))
         sgu[e].copy_(torch.from_numpy(b))
@@ -71,7 +76,8 @@ def metrics(got: np.ndarray, ref: np.ndarray) -> dict:
 class Case:
     """A seeded workload with its routing and the experts it needs."""
 
-    def __init__(self, c: int, T: int | None = None, tokens=None):
+    def __init__(self, c: int, T: int | None = None, tokens=None, fmt: str = "mxfp8"):
+        self.fmt = fmt
         self.w = w = wl.workload(c)
         self.seed = wl.seed_of(c)
         self.T = w.T if T is None else T
@@ -80,7 +86,7 @@ class Case:
         self.ids, self.tw = oracle.route(self.logits, w.k)
         self.tokens = list(range(self.T)) if tokens is None else list(tokens)
         need = np.unique(self.ids[self.tokens])
-        self.experts = wl.make_experts(w, self.seed, need)
+        self.experts = wl.make_experts(w, self.seed, need, fmt=fmt)
 
     def x64(self):
         return wl.bf16_bits_to_f64(self.x_bits)
@@ -88,4 +94,4 @@ class Case:
     def ref(self):
         w = self.w
         return oracle.layer(self.x64(), self.ids, self.tw, self.experts, w.E, w.H, w.I,
-                            tokens=self.tokens)
+                            tokens=self.tokens, fmt=self.fmt)

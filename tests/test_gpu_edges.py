@@ -21,13 +21,14 @@ def dev():
 class Small:
     """A small synthetic layer with every expert generated."""
 
-    def __init__(self, dev, E, k, H, I, T, seed=7, sigma=0.05, flags=0):
+    def __init__(self, dev, E, k, H, I, T, seed=7, sigma=0.05, flags=0, fmt="mxfp8"):
         from sparse_expert_gemv_gb300 import MoEDecode
         self.w = wl.Workload(90, "edge", E, k, H, I, T, sigma)
         self.seed = seed
-        self.experts = wl.make_experts(self.w, seed, range(E))
-        self.wts = device_weights(self.w, self.experts, dev)
-        self.layer = MoEDecode(*self.wts, k=k, max_T=max(T, 1), flags=flags)
+        self.fmt = fmt
+        self.experts = wl.make_experts(self.w, seed, range(E), fmt=fmt)
+        self.wts = device_weights(self.w, self.experts, dev, fmt=fmt)
+        self.layer = MoEDecode(*self.wts, k=k, max_T=max(T, 1), flags=flags, fmt=fmt)
         self.dev = dev
         self.x_bits = wl.make_x(self.w, seed, T)
         self.ids, self.tw = oracle.route(wl.make_logits(self.w, seed, T), k)
@@ -49,7 +50,8 @@ class Small:
         ids = self.ids if ids is None else ids
         tw = self.tw if tw is None else tw
         w = self.w
-        return oracle.layer(wl.bf16_bits_to_f64(x_bits), ids, tw, self.experts, w.E, w.H, w.I)
+        return oracle.layer(wl.bf16_bits_to_f64(x_bits), ids, tw, self.experts, w.E, w.H, w.I,
+                            fmt=self.fmt)
 
     def check(self, **kw):
         h, y = self.run(**kw)
