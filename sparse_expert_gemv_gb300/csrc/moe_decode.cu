@@ -13,6 +13,7 @@
 #include <mutex>
 #include <new>
 
+#include "moe_gate_up_mma.cuh"
 #include "moe_kernels.cuh"
 #include "moe_layer_fused.cuh"
 
@@ -43,6 +44,9 @@ struct moe_decode {
   CUtensorMap tm_scales;          // as tensors for its TMA copies
   CUtensorMap tm_dcodes;
   CUtensorMap tm_dscales;
+  bool gu_tma_ok;                 // the several-token TMA gate/up kernel can run here
+  CUtensorMap tm_gu_codes;        // its W_gateup codes / scales tensor maps
+  CUtensorMap tm_gu_scales;
   uint32_t* d_err;                // device error word (4 bytes) ...
   unsigned long long* d_bar;      // ... then, 8 and 16 bytes on, the fused kernel's launch
                                   // and grid-barrier counters
@@ -95,8 +99,66 @@ constexpr uint32_t kKnownFlags = MOE_FLAG_NO_PDL | MOE_FLAG_HOST_COPY | MOE_FLAG
 
 // ---- gate/up ---------------------------------------------------------------
 
+// Fewest tokens of a gate/up launch that takes moe_gate_up_tma.
+constexpr int kGuTmaMinTokens = 16;
+
+// Weights of a row per ring slot of moe_gate_up_tma: 512 code bytes.
+int gu_tma_kc(const moe_decode* m) { return moe::kGuRowBytes * 32 / code_bytes_per_block(m); }
+
+// Ring slots of moe_gate_up_tma for T tokens: as many as fit beside the
+// staged x (at most 16), 0 when fewer than two fit.
+int gu_tma_slots(const moe_decode* m, int T, size_t& smem) {
+  const moe_decode_config_t& c = m->cfg;
+  const int KC = gu_tma_kc(m), nU_max = std::min(c.E, T * c.k);
+  auto bytes = [&](int SG) { return (size_t)moe::GuTmaSmem(SG, KC, T, c.H, nU_max).total; };
+  if (bytes(2) > m->smem_per_block) return 0;
+  int SG = 2;
+  while (SG < 16 && bytes(SG + 1) <= m->smem_per_block) ++SG;
+  smem = bytes(SG);
+  return SG;
+}
+
+template <int KMAX, class F>
+cudaError_t launch_gate_up_tma(const moe_decode* m, const moe::GateUpParams& p, int SG,
+                               size_t smem, cudaStream_t s) {
+  moe::GateUpTmaParams q;
+  q.tm_codes = m->tm_gu_codes;
+  q.tm_scales = m->tm_gu_scales;
+  q.x = p.x;
+  q.ids = p.ids;
+  q.h = p.h;
+  q.err = p.err;
+  q.T = p.T;
+  q.k = p.k;
+  q.E = p.E;
+  q.H = p.H;
+  q.I = p.I;
+  q.KC = gu_tma_kc(m);
+  q.SG = SG;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(m->num_sms);
+  cfg.blockDim = dim3(moe::kGuThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = use_pdl(m) ? attr : nullptr;
+  cfg.numAttrs = use_pdl(m) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, moe::moe_gate_up_tma<KMAX, F>, q);
+}
+
 template <int NT, int KMAX, class F>
 cudaError_t launch_gate_up_t(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
+  // sixteen or more tokens whose x fits in shared memory beside a weight
+  // ring: tiles streamed by TMA, products on the warp-level MMA (one CTA per
+  // SM). With fewer tokens an expert rarely serves more than one or two, and
+  // the FP32 kernel below issues fewer instructions per weight byte.
+  if (p.T >= kGuTmaMinTokens && m->gu_tma_ok) {
+    size_t smem = 0;
+    const int SG = gu_tma_slots(m, p.T, smem);
+    if (SG >= 2) return launch_gate_up_tma<KMAX, F>(m, p, SG, smem, s);
+  }
   // several tokens whose x fits in shared memory: staged once per CTA as f16
   // blocks (one 16-warp CTA per SM)
   const size_t xs = moe::gate_up_xs_smem(p.T, p.H);
@@ -293,6 +355,22 @@ bool encode_fused_maps(moe_decode* m, int KC, int RC) {
                        (uint64_t)c.H * c.I / 32, RC * c.I / 128, 1);
 }
 
+// The several-token gate/up kernel's tensor maps: W_gateup codes as
+// [E*2I][RB/512][128] uint32 with boxes of 16 rows x 512 bytes, its scales as
+// [E*2I][H/128] uint32 with boxes of 16 rows x KC/32 scale bytes. False when
+// the shape or the scale pointer does not suit them.
+bool encode_gu_tma_maps(moe_decode* m) {
+  const moe_decode_config_t& c = m->cfg;
+  const int KC = gu_tma_kc(m);
+  if (c.H % KC || !aligned(m->sgu, 16)) return false;
+  const int RB = c.H / 32 * code_bytes_per_block(m);
+  const uint64_t rows = (uint64_t)c.E * 2 * c.I;
+  return encode_u32_3d(&m->tm_gu_codes, m->wgu, moe::kGuRowBytes / 4, RB / moe::kGuRowBytes, rows,
+                       RB, 1, moe::kGuRows) &&
+         encode_u32_2d(&m->tm_gu_scales, m->sgu, c.H / 128, rows, c.H / 32, KC / 128,
+                       moe::kGuRows);
+}
+
 cudaError_t set_fused_attributes(size_t smem) {
   cudaError_t e = cudaSuccess;
   for (const void* f : {(const void*)moe::moe_layer_fused_t1<8, moe::Mxfp8>,
@@ -350,8 +428,15 @@ cudaError_t set_xs_attributes_f(size_t smem) {
 }
 
 cudaError_t set_xs_attributes(size_t smem) {
-  const cudaError_t e = set_xs_attributes_f<moe::Mxfp8>(smem);
-  return e == cudaSuccess ? set_xs_attributes_f<moe::Mxfp4>(smem) : e;
+  cudaError_t e = set_xs_attributes_f<moe::Mxfp8>(smem);
+  if (e == cudaSuccess) e = set_xs_attributes_f<moe::Mxfp4>(smem);
+  for (const void* f : {(const void*)moe::moe_gate_up_tma<8, moe::Mxfp8>,
+                        (const void*)moe::moe_gate_up_tma<32, moe::Mxfp8>,
+                        (const void*)moe::moe_gate_up_tma<8, moe::Mxfp4>,
+                        (const void*)moe::moe_gate_up_tma<32, moe::Mxfp4>})
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return e;
 }
 
 bool query_fused(moe_decode* m) {
@@ -509,6 +594,7 @@ moe_status_t moe_decode_create(const moe_decode_config_t* cfg, const uint8_t* w_
                  cudaSuccess;
   m->host_direct = pageable != 0;
   ok = ok && query_fused(m);
+  m->gu_tma_ok = ok && encode_gu_tma_maps(m);
 
 
   ok = ok && set_down_attributes() == cudaSuccess;
@@ -812,6 +898,7 @@ extern "C" moe_status_t moe_decode_layer_noalloc(const moe_decode_config_t* cfg,
                                                                smem) == cudaSuccess &&
                  occ >= 1 && encode_fused_maps(&m, fp.KC, fp.RC);
   }
+  m.gu_tma_ok = encode_gu_tma_maps(&m);
   return moe_decode_layer(&m, T, x, topk_ids, topk_w, reinterpret_cast<uint16_t*>(d.scratch), y,
                           stream);
 }

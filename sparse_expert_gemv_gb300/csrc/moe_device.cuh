@@ -160,6 +160,22 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int x, 
       : "memory");
 }
 
+__host__ __device__ constexpr int round128(int v) { return (v + 127) / 128 * 128; }
+
+// Position in a ring of n shared-memory slots: slot index and the parity of
+// its current fill.
+struct RingPos {
+  int slot, n;
+  uint32_t phase;
+  __device__ __forceinline__ RingPos(int n_) : slot(0), n(n_), phase(0) {}
+  __device__ __forceinline__ void next() {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // Barrier over `nthreads` threads (whole warps) of the CTA on named barrier `id`.
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

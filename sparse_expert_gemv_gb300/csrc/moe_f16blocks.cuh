@@ -208,6 +208,10 @@ __device__ __forceinline__ void f16x2_to_f32(uint32_t w, float& lo, float& hi) {
 //   chunk_f32(q, c, v)   elements 8c .. 8c+7 as FP32
 //   dot_smem(codes, act, lb)  the block's dot with an f16 activation block,
 //                  codes read from shared memory
+//   kLaneBytes, lds_lane(p, w), decode_lane(w, f)  one lane's eight
+//                  consecutive codes of a block (the tensor-core fragment
+//                  layout of moe_gate_up_tma: kLaneBytes bytes in kLaneWords
+//                  words, read from shared memory) and their four f16x2 pairs
 // ---------------------------------------------------------------------------
 
 struct Mxfp8 {
@@ -228,6 +232,18 @@ struct Mxfp8 {
   __device__ __forceinline__ static float dot_smem(const uint8_t* codes, const uint8_t* act,
                                                    const LaneBlock& lb) {
     return dot_block(codes, act, lb);
+  }
+  static constexpr int kLaneBytes = 8;
+  static constexpr int kLaneWords = 2;
+  __device__ __forceinline__ static void lds_lane(const uint8_t* p, uint32_t (&w)[kLaneWords]) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    w[0] = v.x;
+    w[1] = v.y;
+  }
+  __device__ __forceinline__ static void decode_lane(const uint32_t (&w)[kLaneWords],
+                                                     uint32_t (&f)[4]) {
+    e4m3x4_to_f16x2(w[0], f[0], f[1]);
+    e4m3x4_to_f16x2(w[1], f[2], f[3]);
   }
 };
 
@@ -262,6 +278,15 @@ struct Mxfp4 {
     uint32_t wh[16];
     decode(q, lb.c_first != 0, wh);
     return dot_block_h(wh, act, lb);
+  }
+  static constexpr int kLaneBytes = 4;
+  static constexpr int kLaneWords = 1;
+  __device__ __forceinline__ static void lds_lane(const uint8_t* p, uint32_t (&w)[kLaneWords]) {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  }
+  __device__ __forceinline__ static void decode_lane(const uint32_t (&w)[kLaneWords],
+                                                     uint32_t (&f)[4]) {
+    e2m1x8_to_f16x2(w[0], f[0], f[1], f[2], f[3]);
   }
 };
 

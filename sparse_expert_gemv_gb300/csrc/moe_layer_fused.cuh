@@ -91,8 +91,6 @@ struct FusedParams {
   int nrg;      // H / RG: down row granules
 };
 
-__host__ __device__ constexpr int round128(int v) { return (v + 127) / 128 * 128; }
-
 // Byte offsets of a gate/up stage (KB code bytes and KC/32 scale bytes per
 // row) in a ring slot: gate codes, up codes, gate scales, up scales, each
 // region starting on a 128-byte boundary (the TMA tensor copies that fill
@@ -249,19 +247,6 @@ struct DownWalk {
     ng = (nU - u0) < SR ? (nU - u0) : SR;
   }
   __device__ __forceinline__ bool last_group() const { return u0 + ng >= nU; }
-};
-
-// Ring position: slot index and the parity of its current fill.
-struct RingPos {
-  int slot, n;
-  uint32_t phase;
-  __device__ __forceinline__ RingPos(int n_) : slot(0), n(n_), phase(0) {}
-  __device__ __forceinline__ void next() {
-    if (++slot == n) {
-      slot = 0;
-      phase ^= 1u;
-    }
-  }
 };
 
 // Grid barrier of a cooperative launch, in two halves used by one thread per

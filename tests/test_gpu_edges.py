@@ -318,3 +318,36 @@ def test_single_token_layer_barrier_timeout_is_reported(dev):
         _, y = _layer_once(s)
         assert_within(tensor_to_f64(y), r["y_spec"], tol_y(r["y_spec"]), "y after")
     assert s.layer.get_error() == 0
+
+
+# ---------------------------------------------------------------------------
+# sixteen or more tokens with H a multiple of 512 (1024 for MXFP4): the
+# gate/up projection streams 16-neuron tiles with TMA and forms the products
+# on the warp-level MMA, items split over the CTAs (an expert's tokens in
+# passes of eight)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("E,k,H,I,T", [
+    (16, 4, 1024, 256, 20),   # a few tokens per expert
+    (40, 12, 1024, 64, 24),   # k > 8, I = 64: four tiles per expert
+    (6, 2, 1024, 32, 32),     # ~10 tokens per expert: two passes; I = 32
+    (3, 3, 2048, 96, 17),     # every expert serves every token: three passes
+])
+def test_several_token_tma_gate_up(dev, fmt, E, k, H, I, T):
+    s = Small(dev, E, k, H, I, T, seed=E * T, fmt=fmt)
+    s.check()
+    ids = s.ids.copy()
+    ids[0, 1 % k] = ids[0, 0]       # duplicate
+    ids[T - 1, 0] = E + 2           # out of range
+    ids[T // 2, k - 1] = -1
+    h, _ = s.check(ids=ids)
+    hb = tensor_to_f64(h)
+    assert np.all(hb[T - 1, 0] == 0) and np.all(hb[T // 2, k - 1] == 0)
+    from sparse_expert_gemv_gb300 import MOE_DEVICE_BAD_ID
+    assert s.layer.get_error() == MOE_DEVICE_BAD_ID
+    # bitwise reproducible
+    h2, y2 = s.run(ids=ids)
+    h3, y3 = s.run(ids=ids)
+    assert torch.equal(h2.view(torch.int16), h3.view(torch.int16))
+    assert torch.equal(y2.view(torch.int16), y3.view(torch.int16))
