@@ -13,6 +13,7 @@
 #include <mutex>
 #include <new>
 
+#include "moe_down_tma.cuh"
 #include "moe_gate_up_mma.cuh"
 #include "moe_kernels.cuh"
 #include "moe_layer_fused.cuh"
@@ -47,6 +48,9 @@ struct moe_decode {
   bool gu_tma_ok;                 // the several-token TMA gate/up kernel can run here
   CUtensorMap tm_gu_codes;        // its W_gateup codes / scales tensor maps
   CUtensorMap tm_gu_scales;
+  bool dn_tma_ok;                 // the several-token TMA down kernel can run here
+  CUtensorMap tm_dn_codes;        // its W_down codes / scales tensor maps
+  CUtensorMap tm_dn_scales;
   uint32_t* d_err;                // device error word (4 bytes) ...
   unsigned long long* d_bar;      // ... then, 8 and 16 bytes on, the fused kernel's launch
                                   // and grid-barrier counters
@@ -199,7 +203,59 @@ cudaError_t launch_gate_up(const moe_decode* m, const moe::GateUpParams& p, cuda
 
 constexpr int kDownQ = 8;
 
+// Ring slots of moe_down_tma: as many as fit beside h (at most 16), 0 when
+// fewer than two fit.
+int dn_tma_slots(const moe_decode* m, size_t& smem) {
+  const moe_decode_config_t& c = m->cfg;
+  const int IB = c.I / 32 * code_bytes_per_block(m);
+  auto bytes = [&](int SG) { return (size_t)moe::DnTmaSmem(SG, c.I, IB, c.k).total; };
+  if (bytes(2) > m->smem_per_block) return 0;
+  int SG = 2;
+  while (SG < 16 && bytes(SG + 1) <= m->smem_per_block) ++SG;
+  smem = bytes(SG);
+  return SG;
+}
+
+template <class F>
+cudaError_t launch_down_tma(const moe_decode* m, const moe::DownParams& p, int SG, size_t smem,
+                            cudaStream_t s) {
+  moe::DownTmaParams q;
+  q.tm_codes = m->tm_dn_codes;
+  q.tm_scales = m->tm_dn_scales;
+  q.h = p.h;
+  q.ids = p.ids;
+  q.w = p.w;
+  q.y = p.y;
+  q.err = p.err;
+  q.T = p.T;
+  q.k = p.k;
+  q.E = p.E;
+  q.H = p.H;
+  q.I = p.I;
+  q.SG = SG;
+  const long long items = (long long)p.T * (p.H / moe::kDnRows);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min<long long>(items, m->num_sms));
+  cfg.blockDim = dim3(moe::kDnThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = use_pdl(m) ? attr : nullptr;
+  cfg.numAttrs = use_pdl(m) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, moe::moe_down_tma<F>, q);
+}
+
 cudaError_t launch_down(const moe_decode* m, const moe::DownParams& p, cudaStream_t s) {
+  // several tokens: the TMA-streamed kernel, when its maps and ring fit
+  if (p.T >= 2 && m->dn_tma_ok) {
+    size_t smem = 0;
+    const int SG = dn_tma_slots(m, smem);
+    if (SG >= 2)
+      return is_fp4(m) ? launch_down_tma<moe::Mxfp4>(m, p, SG, smem, s)
+                       : launch_down_tma<moe::Mxfp8>(m, p, SG, smem, s);
+  }
   const dim3 grid(p.H / moe::kWarps, p.T), block(moe::kThreads);
   const size_t smem = moe::down_xs_smem(p.k, p.I);
   if (is_fp4(m))
@@ -208,9 +264,16 @@ cudaError_t launch_down(const moe_decode* m, const moe::DownParams& p, cudaStrea
 }
 
 // The down kernels' shared-memory limit: one value for every handle, the
-// library's maximum.
+// library's maximum (the TMA kernels': the device's opt-in maximum).
 cudaError_t set_down_attributes() {
   cudaError_t e = cudaSuccess;
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return cudaErrorUnknown;
+  for (const void* f : {(const void*)moe::moe_down_tma<moe::Mxfp8>,
+                        (const void*)moe::moe_down_tma<moe::Mxfp4>})
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   for (const void* f : {(const void*)moe::moe_down_3d_batched<kDownQ, moe::Mxfp8>,
                         (const void*)moe::moe_down_3d_batched<kDownQ, moe::Mxfp4>})
     if (e == cudaSuccess)
@@ -369,6 +432,21 @@ bool encode_gu_tma_maps(moe_decode* m) {
                        RB, 1, moe::kGuRows) &&
          encode_u32_2d(&m->tm_gu_scales, m->sgu, c.H / 128, rows, c.H / 32, KC / 128,
                        moe::kGuRows);
+}
+
+// The several-token down kernel's tensor maps: W_down codes as
+// [E][H][IB/(4*kin)][kin] uint32 with boxes of one expert's 16 rows, its
+// scales as [E][H*I/128] uint32 with boxes of 16 rows' scale bytes. False
+// when the shape or the pointers do not suit them (I a multiple of 128 and at
+// most 2048, scale array 16-byte aligned).
+bool encode_dn_tma_maps(moe_decode* m) {
+  const moe_decode_config_t& c = m->cfg;
+  if (c.I % 128 || c.I > 2048 || !aligned(m->sd, 16)) return false;
+  const int IB = c.I / 32 * code_bytes_per_block(m);
+  const int kin = std::min(256, IB / 4);
+  return encode_u32_4d(&m->tm_dn_codes, m->wd, kin, IB / (4 * kin), c.H, c.E, moe::kDnRows) &&
+         encode_u32_2d(&m->tm_dn_scales, m->sd, (uint64_t)c.H * c.I / 128, c.E,
+                       (uint64_t)c.H * c.I / 32, moe::kDnRows * c.I / 128, 1);
 }
 
 cudaError_t set_fused_attributes(size_t smem) {
@@ -595,6 +673,7 @@ moe_status_t moe_decode_create(const moe_decode_config_t* cfg, const uint8_t* w_
   m->host_direct = pageable != 0;
   ok = ok && query_fused(m);
   m->gu_tma_ok = ok && encode_gu_tma_maps(m);
+  m->dn_tma_ok = ok && encode_dn_tma_maps(m);
 
 
   ok = ok && set_down_attributes() == cudaSuccess;
@@ -899,6 +978,7 @@ extern "C" moe_status_t moe_decode_layer_noalloc(const moe_decode_config_t* cfg,
                  occ >= 1 && encode_fused_maps(&m, fp.KC, fp.RC);
   }
   m.gu_tma_ok = encode_gu_tma_maps(&m);
+  m.dn_tma_ok = encode_dn_tma_maps(&m);
   return moe_decode_layer(&m, T, x, topk_ids, topk_w, reinterpret_cast<uint16_t*>(d.scratch), y,
                           stream);
 }

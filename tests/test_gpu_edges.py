@@ -351,3 +351,34 @@ def test_several_token_tma_gate_up(dev, fmt, E, k, H, I, T):
     h3, y3 = s.run(ids=ids)
     assert torch.equal(h2.view(torch.int16), h3.view(torch.int16))
     assert torch.equal(y2.view(torch.int16), y3.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# two or more tokens with I a multiple of 128 (at most 2048): the down
+# projection streams each distinct routed expert's 16-row tiles with TMA,
+# one warp per output row
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("E,k,H,I,T", [
+    (8, 2, 256, 128, 2),      # the smallest tile counts
+    (12, 10, 512, 384, 9),    # k > 8
+    (20, 4, 96, 2048, 3),     # I at its maximum, six row tiles
+    (6, 3, 256, 128, 40),     # T > 32: two token groups
+])
+def test_several_token_tma_down(dev, fmt, E, k, H, I, T):
+    s = Small(dev, E, k, H, I, T, seed=3 * E + T, fmt=fmt)
+    s.check()
+    ids = s.ids.copy()
+    ids[0, 1] = ids[0, 0]           # duplicate: one distinct expert, weights summed
+    ids[T - 1, :] = ids[T - 1, 0]   # every slot the same expert
+    ids[T // 2, k - 1] = E          # out of range
+    _, y = s.check(ids=ids)
+    from sparse_expert_gemv_gb300 import MOE_DEVICE_BAD_ID
+    assert s.layer.get_error() == MOE_DEVICE_BAD_ID
+    # every id of a token invalid: its y row is zero
+    ids[1, :] = -1
+    _, y = s.check(ids=ids)
+    assert torch.count_nonzero(y[1]).item() == 0
+    _, y2 = s.run(ids=ids)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
