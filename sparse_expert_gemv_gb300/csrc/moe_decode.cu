@@ -13,6 +13,7 @@
 #include <mutex>
 #include <new>
 
+#include "moe_down_mma.cuh"
 #include "moe_down_tma.cuh"
 #include "moe_gate_up_mma.cuh"
 #include "moe_kernels.cuh"
@@ -247,8 +248,72 @@ cudaError_t launch_down_tma(const moe_decode* m, const moe::DownParams& p, int S
   return cudaLaunchKernelEx(&cfg, moe::moe_down_tma<F>, q);
 }
 
+// Fewest ring slots (and so reducing warps) with which moe_down_mma is used.
+constexpr int kDnMmaMinSlots = 6;
+
+// Ring slots of moe_down_mma for T tokens: as many as fit, at most one per
+// consumer warp; 0 when fewer than two fit.
+int dn_mma_slots(const moe_decode* m, int T, size_t& smem) {
+  const moe_decode_config_t& c = m->cfg;
+  const int IB = c.I / 32 * code_bytes_per_block(m), nU_max = std::min(c.E, T * c.k);
+  auto bytes = [&](int SG) { return (size_t)moe::DmSmem(SG, c.I, IB, T, nU_max).total; };
+  if (bytes(2) > m->smem_per_block) return 0;
+  int SG = 2;
+  while (SG < moe::kDmConsumers && bytes(SG + 1) <= m->smem_per_block) ++SG;
+  smem = bytes(SG);
+  return SG;
+}
+
+template <int KMAX, class F>
+cudaError_t launch_down_mma(const moe_decode* m, const moe::DownParams& p, int SG, size_t smem,
+                            cudaStream_t s) {
+  moe::DownMmaParams q;
+  q.tm_codes = m->tm_dn_codes;
+  q.tm_scales = m->tm_dn_scales;
+  q.h = p.h;
+  q.ids = p.ids;
+  q.w = p.w;
+  q.y = p.y;
+  q.err = p.err;
+  q.T = p.T;
+  q.k = p.k;
+  q.E = p.E;
+  q.H = p.H;
+  q.I = p.I;
+  q.SG = SG;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min(p.H / moe::kDmRows, m->num_sms));
+  cfg.blockDim = dim3(moe::kDmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = use_pdl(m) ? attr : nullptr;
+  cfg.numAttrs = use_pdl(m) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, moe::moe_down_mma<KMAX, F>, q);
+}
+
+template <class F>
+cudaError_t launch_down_mma_k(const moe_decode* m, const moe::DownParams& p, int SG, size_t smem,
+                              cudaStream_t s) {
+  return p.k <= 8 ? launch_down_mma<8, F>(m, p, SG, smem, s) : launch_down_mma<32, F>(m, p, SG, smem, s);
+}
+
 cudaError_t launch_down(const moe_decode* m, const moe::DownParams& p, cudaStream_t s) {
-  // several tokens: the TMA-streamed kernel, when its maps and ring fit
+  // sixteen or more tokens with rows of at most 1 KB of codes: each unique
+  // expert's row tiles streamed once, products on the warp-level MMA (with
+  // fewer tokens an expert rarely serves more than one or two, and the
+  // token-by-token kernel below keeps more of the stream in flight)
+  if (p.T >= kGuTmaMinTokens && m->dn_tma_ok && p.I / 32 * code_bytes_per_block(m) <= 1024) {
+    // (a warp per ring slot: with few slots too few warps would reduce)
+    size_t smem = 0;
+    const int SG = dn_mma_slots(m, p.T, smem);
+    if (SG >= kDnMmaMinSlots)
+      return is_fp4(m) ? launch_down_mma_k<moe::Mxfp4>(m, p, SG, smem, s)
+                       : launch_down_mma_k<moe::Mxfp8>(m, p, SG, smem, s);
+  }
+  // several tokens otherwise: the TMA-streamed kernel, token by token
   if (p.T >= 2 && m->dn_tma_ok) {
     size_t smem = 0;
     const int SG = dn_tma_slots(m, smem);
@@ -272,7 +337,11 @@ cudaError_t set_down_attributes() {
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return cudaErrorUnknown;
   for (const void* f : {(const void*)moe::moe_down_tma<moe::Mxfp8>,
-                        (const void*)moe::moe_down_tma<moe::Mxfp4>})
+                        (const void*)moe::moe_down_tma<moe::Mxfp4>,
+                        (const void*)moe::moe_down_mma<8, moe::Mxfp8>,
+                        (const void*)moe::moe_down_mma<32, moe::Mxfp8>,
+                        (const void*)moe::moe_down_mma<8, moe::Mxfp4>,
+                        (const void*)moe::moe_down_mma<32, moe::Mxfp4>})
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   for (const void* f : {(const void*)moe::moe_down_3d_batched<kDownQ, moe::Mxfp8>,
                         (const void*)moe::moe_down_3d_batched<kDownQ, moe::Mxfp4>})
