@@ -367,7 +367,7 @@ def run_ours(args, rank, world, local):
         achieved = float(bytes_step[W:].mean()) / launch_s / 1e9
         launches = K
     else:
-        kernel = "moe_gate_up_3d_batched"
+        kernel = layers[0][1].kernel_name(T, "gate_up")
         launch_s = dt_gu / K
         achieved = float(bytes_gu[W:].mean()) / launch_s / 1e9
         launches = 2 * K

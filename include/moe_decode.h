@@ -221,6 +221,17 @@ int32_t moe_decode_version(void);
 int32_t moe_decode_fused_layer(moe_decode_t handle);
 
 /*
+ * Diagnostic: the name of the kernel that moe_gate_up (which = 0) or moe_down
+ * (which = 1) launches for T tokens on this handle (for T > 32, for each
+ * group of 32): "moe_gate_up_tma", "moe_gate_up_3d_batched_xs" or
+ * "moe_gate_up_3d_batched"; "moe_down_mma", "moe_down_tma" or
+ * "moe_down_3d_batched". A static string; "" for a NULL handle, T <= 0 or
+ * another `which`. (moe_decode_layer with T = 1 uses moe_layer_fused_t1 when
+ * moe_decode_fused_layer says so.)
+ */
+const char* moe_decode_kernel_name(moe_decode_t handle, int32_t T, int32_t which);
+
+/*
  * Test support for failure detection (the pages have no counterpart): moves
  * this handle's launch counter far ahead of its grid-barrier counter, so that
  * the next one-launch call's grid barrier can never be met. Every CTA's

@@ -60,6 +60,7 @@ SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [_st]),
     "moe_decode_version": (_i32, []),
     "moe_decode_fused_layer": (_i32, [_p]),
+    "moe_decode_kernel_name": (ctypes.c_char_p, [_p, _i32, _i32]),
     "moe_decode_arm_barrier_timeout": (_st, [_p]),
     "moe_decode_layer_noalloc": (_st, [ctypes.POINTER(MoEConfig), _p, _p, _p, _p, _i32, _p, _p, _p,
                                        _p, _p]),

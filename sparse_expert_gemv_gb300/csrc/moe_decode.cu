@@ -153,21 +153,33 @@ cudaError_t launch_gate_up_tma(const moe_decode* m, const moe::GateUpParams& p, 
   return cudaLaunchKernelEx(&cfg, moe::moe_gate_up_tma<KMAX, F>, q);
 }
 
-template <int NT, int KMAX, class F>
-cudaError_t launch_gate_up_t(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
+// The gate/up kernel of a launch of T tokens (at most 32), with its ring
+// slots and shared memory where it has a ring.
+enum class GuKind { kTma, kXs, kL1 };
+GuKind gate_up_kind(const moe_decode* m, int T, int& SG, size_t& smem) {
   // sixteen or more tokens whose x fits in shared memory beside a weight
   // ring: tiles streamed by TMA, products on the warp-level MMA (one CTA per
   // SM). With fewer tokens an expert rarely serves more than one or two, and
   // the FP32 kernel below issues fewer instructions per weight byte.
-  if (p.T >= kGuTmaMinTokens && m->gu_tma_ok) {
-    size_t smem = 0;
-    const int SG = gu_tma_slots(m, p.T, smem);
-    if (SG >= 2) return launch_gate_up_tma<KMAX, F>(m, p, SG, smem, s);
+  if (T >= kGuTmaMinTokens && m->gu_tma_ok) {
+    SG = gu_tma_slots(m, T, smem);
+    if (SG >= 2) return GuKind::kTma;
   }
   // several tokens whose x fits in shared memory: staged once per CTA as f16
   // blocks (one 16-warp CTA per SM)
-  const size_t xs = moe::gate_up_xs_smem(p.T, p.H);
-  if (p.T >= 2 && xs <= m->smem_per_block) {
+  smem = moe::gate_up_xs_smem(T, m->cfg.H);
+  if (T >= 2 && smem <= m->smem_per_block) return GuKind::kXs;
+  return GuKind::kL1;
+}
+
+template <int NT, int KMAX, class F>
+cudaError_t launch_gate_up_t(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
+  int SG = 0;
+  size_t smem = 0;
+  const GuKind kind = gate_up_kind(m, p.T, SG, smem);
+  if (kind == GuKind::kTma) return launch_gate_up_tma<KMAX, F>(m, p, SG, smem, s);
+  if (kind == GuKind::kXs) {
+    const size_t xs = smem;
     const long long units_max = (long long)std::min(p.E, p.T * p.k) * p.I;
     const long long ctas_needed = (units_max + moe::kXsWarps - 1) / moe::kXsWarps;
     const int grid = (int)std::max(1LL, std::min(ctas_needed, (long long)m->num_sms));
@@ -251,6 +263,31 @@ cudaError_t launch_down_tma(const moe_decode* m, const moe::DownParams& p, int S
 // Fewest ring slots (and so reducing warps) with which moe_down_mma is used.
 constexpr int kDnMmaMinSlots = 6;
 
+int dn_tma_slots(const moe_decode* m, size_t& smem);
+int dn_mma_slots(const moe_decode* m, int T, size_t& smem);
+
+// The down kernel of a launch of T tokens (at most 32), with its ring slots
+// and shared memory where it has a ring.
+enum class DnKind { kMma, kTma, kWarp };
+DnKind down_kind(const moe_decode* m, int T, int& SG, size_t& smem) {
+  // sixteen or more tokens with rows of at most 1 KB of codes: each unique
+  // expert's row tiles streamed once, products on the warp-level MMA (with
+  // fewer tokens an expert rarely serves more than one or two, and the
+  // token-by-token kernel keeps more of the stream in flight; a warp per ring
+  // slot: with few slots too few warps would reduce)
+  if (T >= kGuTmaMinTokens && m->dn_tma_ok && m->cfg.I / 32 * code_bytes_per_block(m) <= 1024) {
+    SG = dn_mma_slots(m, T, smem);
+    if (SG >= kDnMmaMinSlots) return DnKind::kMma;
+  }
+  // several tokens otherwise: the TMA-streamed kernel, token by token
+  if (T >= 2 && m->dn_tma_ok) {
+    SG = dn_tma_slots(m, smem);
+    if (SG >= 2) return DnKind::kTma;
+  }
+  smem = moe::down_xs_smem(m->cfg.k, m->cfg.I);
+  return DnKind::kWarp;
+}
+
 // Ring slots of moe_down_mma for T tokens: as many as fit, at most one per
 // consumer warp; 0 when fewer than two fit.
 int dn_mma_slots(const moe_decode* m, int T, size_t& smem) {
@@ -301,28 +338,16 @@ cudaError_t launch_down_mma_k(const moe_decode* m, const moe::DownParams& p, int
 }
 
 cudaError_t launch_down(const moe_decode* m, const moe::DownParams& p, cudaStream_t s) {
-  // sixteen or more tokens with rows of at most 1 KB of codes: each unique
-  // expert's row tiles streamed once, products on the warp-level MMA (with
-  // fewer tokens an expert rarely serves more than one or two, and the
-  // token-by-token kernel below keeps more of the stream in flight)
-  if (p.T >= kGuTmaMinTokens && m->dn_tma_ok && p.I / 32 * code_bytes_per_block(m) <= 1024) {
-    // (a warp per ring slot: with few slots too few warps would reduce)
-    size_t smem = 0;
-    const int SG = dn_mma_slots(m, p.T, smem);
-    if (SG >= kDnMmaMinSlots)
-      return is_fp4(m) ? launch_down_mma_k<moe::Mxfp4>(m, p, SG, smem, s)
-                       : launch_down_mma_k<moe::Mxfp8>(m, p, SG, smem, s);
-  }
-  // several tokens otherwise: the TMA-streamed kernel, token by token
-  if (p.T >= 2 && m->dn_tma_ok) {
-    size_t smem = 0;
-    const int SG = dn_tma_slots(m, smem);
-    if (SG >= 2)
-      return is_fp4(m) ? launch_down_tma<moe::Mxfp4>(m, p, SG, smem, s)
-                       : launch_down_tma<moe::Mxfp8>(m, p, SG, smem, s);
-  }
+  int SG = 0;
+  size_t smem = 0;
+  const DnKind kind = down_kind(m, p.T, SG, smem);
+  if (kind == DnKind::kMma)
+    return is_fp4(m) ? launch_down_mma_k<moe::Mxfp4>(m, p, SG, smem, s)
+                     : launch_down_mma_k<moe::Mxfp8>(m, p, SG, smem, s);
+  if (kind == DnKind::kTma)
+    return is_fp4(m) ? launch_down_tma<moe::Mxfp4>(m, p, SG, smem, s)
+                     : launch_down_tma<moe::Mxfp8>(m, p, SG, smem, s);
   const dim3 grid(p.H / moe::kWarps, p.T), block(moe::kThreads);
-  const size_t smem = moe::down_xs_smem(p.k, p.I);
   if (is_fp4(m))
     return launch(moe::moe_down_3d_batched<kDownQ, moe::Mxfp4>, grid, block, smem, s, use_pdl(m), p);
   return launch(moe::moe_down_3d_batched<kDownQ, moe::Mxfp8>, grid, block, smem, s, use_pdl(m), p);
@@ -921,6 +946,27 @@ const char* moe_status_string(moe_status_t status) {
 int32_t moe_decode_version(void) { return kVersion; }
 
 int32_t moe_decode_fused_layer(moe_decode_t m) { return m ? (m->fused_ok ? 1 : 0) : -1; }
+
+const char* moe_decode_kernel_name(moe_decode_t m, int32_t T, int32_t which) {
+  if (!m || T <= 0 || (which != 0 && which != 1)) return "";
+  const int Tl = std::min<int>(T, moe::kMaxTokensPerLaunch);
+  int SG = 0;
+  size_t smem = 0;
+  if (which == 0) {
+    switch (gate_up_kind(m, Tl, SG, smem)) {
+      case GuKind::kTma: return "moe_gate_up_tma";
+      case GuKind::kXs: return "moe_gate_up_3d_batched_xs";
+      case GuKind::kL1: return "moe_gate_up_3d_batched";
+    }
+    return "";
+  }
+  switch (down_kind(m, Tl, SG, smem)) {
+    case DnKind::kMma: return "moe_down_mma";
+    case DnKind::kTma: return "moe_down_tma";
+    case DnKind::kWarp: return "moe_down_3d_batched";
+  }
+  return "";
+}
 
 moe_status_t moe_decode_arm_barrier_timeout(moe_decode_t m) {
   if (!m) return MOE_ERR_INVALID_ARG;

@@ -102,6 +102,12 @@ class MoEDecode:
         """True when one-token layer calls run as one persistent launch."""
         return lib.moe_decode_fused_layer(self._h) == 1
 
+    def kernel_name(self, T: int, which: str) -> str:
+        """The kernel moe_gate_up (which="gate_up") or moe_down ("down")
+        launches for T tokens on this handle."""
+        w = {"gate_up": 0, "down": 1}[which]
+        return lib.moe_decode_kernel_name(self._h, T, w).decode()
+
     def arm_barrier_timeout(self) -> None:
         """Test support: the next one-launch call's grid barrier times out
         (bounded; it sets MOE_DEVICE_TIMEOUT, which get_error reports)."""

@@ -336,6 +336,7 @@ def test_single_token_layer_barrier_timeout_is_reported(dev):
 ])
 def test_several_token_tma_gate_up(dev, fmt, E, k, H, I, T):
     s = Small(dev, E, k, H, I, T, seed=E * T, fmt=fmt)
+    assert s.layer.kernel_name(T, "gate_up") == "moe_gate_up_tma"
     s.check()
     ids = s.ids.copy()
     ids[0, 1 % k] = ids[0, 0]       # duplicate
@@ -368,6 +369,9 @@ def test_several_token_tma_gate_up(dev, fmt, E, k, H, I, T):
 ])
 def test_several_token_tma_down(dev, fmt, E, k, H, I, T):
     s = Small(dev, E, k, H, I, T, seed=3 * E + T, fmt=fmt)
+    # fewer than 16 tokens: token by token; 16 or more (here a group of 32):
+    # each unique expert's rows once, on the MMA
+    assert s.layer.kernel_name(T, "down") == ("moe_down_mma" if T >= 16 else "moe_down_tma")
     s.check()
     ids = s.ids.copy()
     ids[0, 1] = ids[0, 0]           # duplicate: one distinct expert, weights summed
@@ -382,3 +386,23 @@ def test_several_token_tma_down(dev, fmt, E, k, H, I, T):
     assert torch.count_nonzero(y[1]).item() == 0
     _, y2 = s.run(ids=ids)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+def test_kernel_choice_by_workload(dev):
+    # which kernels the seeded workloads' calls take (weights need not be real)
+    from sparse_expert_gemv_gb300 import MoEDecode
+    want = {
+        0: ("moe_gate_up_3d_batched", "moe_down_3d_batched"),       # T = 1, shapes below the ring kernels
+        1: ("moe_gate_up_3d_batched", "moe_down_3d_batched"),       # T = 1 (moe_decode_layer: one launch)
+        2: ("moe_gate_up_3d_batched_xs", "moe_down_tma"),
+        3: ("moe_gate_up_tma", "moe_down_mma"),
+    }
+    for c, (gu, dn) in want.items():
+        w = wl.workload(c)
+        for fmt in ("mxfp8", "mxfp4"):
+            lay = MoEDecode(*device_weights(w, {}, dev, fmt=fmt), k=w.k, max_T=w.T, fmt=fmt)
+            assert lay.kernel_name(w.T, "gate_up") == gu, (c, fmt)
+            assert lay.kernel_name(w.T, "down") == dn, (c, fmt)
+            # the one-launch single-token form depends on the shape alone
+            assert lay.fused_single_token == (c != 0), (c, fmt)
+            lay.close()
