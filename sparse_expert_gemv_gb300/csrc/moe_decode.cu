@@ -460,9 +460,11 @@ bool encode_u32_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t ro
 }
 
 // A [rows, n1, n0] uint32 tensor (n0 innermost, rows `pitch` bytes apart),
-// read in boxes of box_rows x b1 x n0.
+// read in boxes of box_rows x b1 x n0, written to shared memory as is or
+// with the 128-byte swizzle (then n0 * 4 must be 128).
 bool encode_u32_3d(CUtensorMap* tm, const void* base, uint64_t n0, uint64_t n1, uint64_t rows,
-                   uint64_t pitch, uint32_t b1, uint32_t box_rows) {
+                   uint64_t pitch, uint32_t b1, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[3] = {n0, n1, rows};
@@ -470,8 +472,8 @@ bool encode_u32_3d(CUtensorMap* tm, const void* base, uint64_t n0, uint64_t n1, 
   cuuint32_t box[3] = {(cuuint32_t)n0, b1, box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // A [n3, n2, n1, n0] uint32 tensor (n0 innermost, dense), read in boxes of
@@ -513,17 +515,18 @@ bool encode_fused_maps(moe_decode* m, int KC, int RC) {
 }
 
 // The several-token gate/up kernel's tensor maps: W_gateup codes as
-// [E*2I][RB/512][128] uint32 with boxes of 16 rows x 512 bytes, its scales as
-// [E*2I][H/128] uint32 with boxes of 16 rows x KC/32 scale bytes. False when
-// the shape or the scale pointer does not suit them.
+// [E*2I][RB/128][32] uint32 with boxes of 16 rows x 128 bytes written with
+// the 128-byte swizzle, its scales as [E*2I][H/128] uint32 with boxes of 16
+// rows x KC/32 scale bytes. False when the shape or the scale pointer does
+// not suit them.
 bool encode_gu_tma_maps(moe_decode* m) {
   const moe_decode_config_t& c = m->cfg;
   const int KC = gu_tma_kc(m);
   if (c.H % KC || !aligned(m->sgu, 16)) return false;
   const int RB = c.H / 32 * code_bytes_per_block(m);
   const uint64_t rows = (uint64_t)c.E * 2 * c.I;
-  return encode_u32_3d(&m->tm_gu_codes, m->wgu, moe::kGuRowBytes / 4, RB / moe::kGuRowBytes, rows,
-                       RB, 1, moe::kGuRows) &&
+  return encode_u32_3d(&m->tm_gu_codes, m->wgu, 32, RB / 128, rows, RB, 1, moe::kGuRows,
+                       CU_TENSOR_MAP_SWIZZLE_128B) &&
          encode_u32_2d(&m->tm_gu_scales, m->sgu, c.H / 128, rows, c.H / 32, KC / 128,
                        moe::kGuRows);
 }

@@ -69,25 +69,41 @@ struct GateUpTmaParams {
   int SG;                 // ring slots
 };
 
-// Byte offsets of one ring slot: gate codes [16][512], up codes [16][512],
-// gate scales [16][KC/32], up scales [16][KC/32] (128-byte aligned regions).
+// A ring slot is a code slot (1024-byte aligned: gate codes, then up codes)
+// and a scale slot (gate scales [16][KC/32], then up scales). Each matrix's
+// codes are four [16][128] pieces (row bytes 0-127, 128-255, ...) written by
+// TMA with the 128-byte swizzle: 16-byte chunk j of row r sits at chunk
+// j ^ (r % 8), so the 16 rows' chunks a warp reads at once fall in
+// different banks.
 struct GuSlot {
-  int gs, us, end;
+  int codes, us, scales;   // code slot bytes, up scales' offset, scale slot bytes
   __host__ __device__ explicit GuSlot(int KC)
-      : gs(2 * kGuRows * kGuRowBytes),
-        us(2 * kGuRows * kGuRowBytes + round128(kGuRows * (KC >> 5))),
-        end(2 * kGuRows * kGuRowBytes + 2 * round128(kGuRows * (KC >> 5))) {}
+      : codes(2 * kGuRows * kGuRowBytes),
+        us(round128(kGuRows * (KC >> 5))),
+        scales(2 * round128(kGuRows * (KC >> 5))) {}
 };
+
+// Address of byte o (< 512) of row r of a matrix's codes in a slot.
+__device__ __forceinline__ const uint8_t* gu_code(const uint8_t* m, int r, int o) {
+  return m + (o >> 7) * (kGuRows * 128) + r * 128 + ((((o >> 4) & 7) ^ (r & 7)) << 4) + (o & 15);
+}
 
 // Shared-memory map (byte offsets, 128-byte aligned): the ring, x as f16
 // rows, their block factors, two buffers for the warps' partial sums, the
 // mbarriers, the warps' schedule words, each consumer warp's token list of
 // its current item, and the prefix counts of items.
 struct GuTmaSmem {
-  int slot, xs, xf, red, bars, words, tl, pref, total;
+  int slot, sslot, sc, xs, xf, red, bars, words, tl, pref, total;
+  // offsets from the first 1024-byte boundary of the dynamic shared memory
+  // (total includes the up to 1024 bytes before it); the code slots first,
+  // then the scale slots
   __host__ __device__ GuTmaSmem(int SG, int KC, int T, int H, int nU_max) {
-    slot = GuSlot(KC).end;
+    const GuSlot gs(KC);
+    slot = gs.codes;
+    sslot = gs.scales;
     int o = SG * slot;
+    sc = o;
+    o += SG * sslot;
     xs = o;
     o += round128(T * mma_xrow(H));
     xf = o;
@@ -102,7 +118,7 @@ struct GuTmaSmem {
     o += kGuConsumers * 2 * kGuTokens * 4;
     pref = o;
     o += round128((nU_max + 1) * 4);
-    total = o;
+    total = o + 1024;
   }
 };
 
@@ -159,7 +175,9 @@ struct GuItems {
 
 template <int KMAX, class F>
 __global__ void __launch_bounds__(kGuThreads, 1) moe_gate_up_tma(const __grid_constant__ GateUpTmaParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // the swizzled TMA copies need 1024-byte aligned destinations
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   constexpr int CB = F::kBlockBytes, LB = F::kLaneBytes;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -170,6 +188,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gate_up_tma(const __grid_co
   const int nU_max = min(p.E, p.T * p.k);
   const GuTmaSmem L(SG, KC, p.T, H, nU_max);
   const GuSlot sl(KC);
+  uint8_t* sring = smem + L.sc;
   uint8_t* ring = smem;
   uint8_t* xs = smem + L.xs;
   float* xf = reinterpret_cast<float*>(smem + L.xf);
@@ -262,10 +281,15 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gate_up_tma(const __grid_co
           uint8_t* dst = ring + (size_t)rg.slot * L.slot;
           uint64_t* bar = &full[rg.slot];
           mbar_expect_tx(bar, 2u * kGuRows * kGuRowBytes + 2u * kGuRows * (KC >> 5));
-          tma_load_3d(dst, &p.tm_codes, 0, kc, row, bar);
-          tma_load_3d(dst + kGuRows * kGuRowBytes, &p.tm_codes, 0, kc, row + I, bar);
-          tma_load_2d(dst + sl.gs, &p.tm_scales, kc * (KC >> 7), row, bar);
-          tma_load_2d(dst + sl.us, &p.tm_scales, kc * (KC >> 7), row + I, bar);
+          for (int q = 0; q < kGuRowBytes / 128; ++q) {
+            tma_load_3d(dst + q * kGuRows * 128, &p.tm_codes, 0, kc * (kGuRowBytes / 128) + q, row,
+                        bar);
+            tma_load_3d(dst + kGuRows * kGuRowBytes + q * kGuRows * 128, &p.tm_codes, 0,
+                        kc * (kGuRowBytes / 128) + q, row + I, bar);
+          }
+          uint8_t* sdst = sring + (size_t)rg.slot * L.sslot;
+          tma_load_2d(sdst, &p.tm_scales, kc * (KC >> 7), row, bar);
+          tma_load_2d(sdst + sl.us, &p.tm_scales, kc * (KC >> 7), row + I, bar);
         }
       }
     }
@@ -324,26 +348,28 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gate_up_tma(const __grid_co
       if (!dead) dead = !mbar_wait(&full[rg.slot], rg.phase, p.err);
       if (!dead) {
         const uint8_t* st = ring + (size_t)rg.slot * L.slot;
+        const uint8_t* ss = sring + (size_t)rg.slot * L.sslot;
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
           if (bi < bpw) {
             const int blk = warp * bpw + bi;          // block within the slot
             const int b = kc * nbk + blk;             // block of the row
-            const uint8_t* cg0 = st + g * kGuRowBytes + blk * CB + c * LB;
+            const int o = blk * CB + c * LB;             // byte of the slot's row chunk
+            const uint8_t* upm = st + kGuRows * kGuRowBytes;
             uint32_t q[4][F::kLaneWords];
-            F::lds_lane(cg0, q[0]);
-            F::lds_lane(cg0 + 8 * kGuRowBytes, q[1]);
-            F::lds_lane(cg0 + kGuRows * kGuRowBytes, q[2]);
-            F::lds_lane(cg0 + (kGuRows + 8) * kGuRowBytes, q[3]);
+            F::lds_lane(gu_code(st, g, o), q[0]);
+            F::lds_lane(gu_code(st, g + 8, o), q[1]);
+            F::lds_lane(gu_code(upm, g, o), q[2]);
+            F::lds_lane(gu_code(upm, g + 8, o), q[3]);
             uint32_t fg0[4], fg1[4], fu0[4], fu1[4];
             F::decode_lane(q[0], fg0);
             F::decode_lane(q[1], fg1);
             F::decode_lane(q[2], fu0);
             F::decode_lane(q[3], fu1);
-            const float s_g0 = ue8m0_to_f32(st[sl.gs + g * nbk + blk]);
-            const float s_g1 = ue8m0_to_f32(st[sl.gs + (g + 8) * nbk + blk]);
-            const float s_u0 = ue8m0_to_f32(st[sl.us + g * nbk + blk]);
-            const float s_u1 = ue8m0_to_f32(st[sl.us + (g + 8) * nbk + blk]);
+            const float s_g0 = ue8m0_to_f32(ss[g * nbk + blk]);
+            const float s_g1 = ue8m0_to_f32(ss[(g + 8) * nbk + blk]);
+            const float s_u0 = ue8m0_to_f32(ss[sl.us + g * nbk + blk]);
+            const float s_u1 = ue8m0_to_f32(ss[sl.us + (g + 8) * nbk + blk]);
             const uint4 xb = tok_g >= 0 ? *reinterpret_cast<const uint4*>(xrow_g + 64 * b)
                                         : make_uint4(0u, 0u, 0u, 0u);
             const float fa = tok_a >= 0 ? xf_a[b] : 0.f;
