@@ -672,12 +672,31 @@ moe_status_t fused_layer(moe_decode* m, const uint16_t* x, const int32_t* ids, c
 
 // ---- per-call token chunking -----------------------------------------------
 
+// Tokens per gate/up launch: groups of 32, or, when a group's x does not fit
+// in shared memory (the kernel that reads x through L1 would run) but that of
+// a group of at least four does, groups of the largest such size. Each group
+// streams its unique experts once, so smaller groups read an expert shared
+// between groups more than once; the staged kernel more than pays for that.
+int gate_up_group(const moe_decode* m, int T) {
+  int g = std::min(T, moe::kMaxTokensPerLaunch);
+  int SG = 0;
+  size_t smem = 0;
+  if (g < 2 || gate_up_kind(m, g, SG, smem) != GuKind::kL1) return g;
+  int g2 = g;
+  while (g2 > 4 && moe::gate_up_xs_smem(g2, m->cfg.H) > m->smem_per_block) --g2;
+  if (moe::gate_up_xs_smem(g2, m->cfg.H) > m->smem_per_block) return g;
+  // equal groups: T = 16 with room for 15 runs as two groups of 8
+  const int n = (T + g2 - 1) / g2;
+  return (T + n - 1) / n;
+}
+
 moe_status_t gate_up_chunks(moe_decode* m, int T, const uint16_t* x, const int32_t* ids,
                             uint16_t* h, cudaStream_t s) {
   const moe_decode_config_t& c = m->cfg;
-  for (int t0 = 0; t0 < T; t0 += moe::kMaxTokensPerLaunch) {
+  const int G = gate_up_group(m, T);
+  for (int t0 = 0; t0 < T; t0 += G) {
     moe::GateUpParams p;
-    p.T = std::min(moe::kMaxTokensPerLaunch, T - t0);
+    p.T = std::min(G, T - t0);
     p.x = x + (size_t)t0 * c.H;
     p.ids = ids + (size_t)t0 * c.k;
     p.h = h + (size_t)t0 * c.k * c.I;
@@ -956,7 +975,7 @@ const char* moe_decode_kernel_name(moe_decode_t m, int32_t T, int32_t which) {
   int SG = 0;
   size_t smem = 0;
   if (which == 0) {
-    switch (gate_up_kind(m, Tl, SG, smem)) {
+    switch (gate_up_kind(m, gate_up_group(m, T), SG, smem)) {
       case GuKind::kTma: return "moe_gate_up_tma";
       case GuKind::kXs: return "moe_gate_up_3d_batched_xs";
       case GuKind::kL1: return "moe_gate_up_3d_batched";
