@@ -172,6 +172,16 @@ GuKind gate_up_kind(const moe_decode* m, int T, int& SG, size_t& smem) {
   return GuKind::kL1;
 }
 
+template <int NT, int KMAX, class F, int D>
+cudaError_t launch_gate_up_xs(const moe_decode* m, const moe::GateUpParams& p, size_t xs,
+                              cudaStream_t s) {
+  const long long units_max = (long long)std::min(p.E, p.T * p.k) * p.I;
+  const long long ctas_needed = (units_max + moe::kXsWarps - 1) / moe::kXsWarps;
+  const int grid = (int)std::max(1LL, std::min(ctas_needed, (long long)m->num_sms));
+  return launch(moe::moe_gate_up_3d_batched_xs<NT, KMAX, F, D>, dim3(grid), dim3(moe::kXsThreads),
+                xs, s, use_pdl(m), p);
+}
+
 template <int NT, int KMAX, class F>
 cudaError_t launch_gate_up_t(const moe_decode* m, const moe::GateUpParams& p, cudaStream_t s) {
   int SG = 0;
@@ -179,12 +189,11 @@ cudaError_t launch_gate_up_t(const moe_decode* m, const moe::GateUpParams& p, cu
   const GuKind kind = gate_up_kind(m, p.T, SG, smem);
   if (kind == GuKind::kTma) return launch_gate_up_tma<KMAX, F>(m, p, SG, smem, s);
   if (kind == GuKind::kXs) {
-    const size_t xs = smem;
-    const long long units_max = (long long)std::min(p.E, p.T * p.k) * p.I;
-    const long long ctas_needed = (units_max + moe::kXsWarps - 1) / moe::kXsWarps;
-    const int grid = (int)std::max(1LL, std::min(ctas_needed, (long long)m->num_sms));
-    return launch(moe::moe_gate_up_3d_batched_xs<NT, KMAX, F>, dim3(grid), dim3(moe::kXsThreads), xs,
-                  s, use_pdl(m), p);
+    // at most one token per expert on average (T*k <= E): token groups of two
+    // and two weight blocks per lane in flight (the registers of larger
+    // token groups go to the stream instead)
+    if ((long long)p.T * p.k <= p.E) return launch_gate_up_xs<2, KMAX, F, 2>(m, p, smem, s);
+    return launch_gate_up_xs<NT, KMAX, F, 1>(m, p, smem, s);
   }
   const long long units_max = (long long)std::min(p.E, p.T * p.k) * p.I;
   const long long ctas_needed = (units_max + moe::kWarps - 1) / moe::kWarps;
@@ -589,14 +598,16 @@ cudaError_t launch_fused(const moe_decode* m, const moe::FusedParams& fp, size_t
 template <class F>
 cudaError_t set_xs_attributes_f(size_t smem) {
   cudaError_t e = cudaSuccess;
-  for (const void* f : {(const void*)moe::moe_gate_up_3d_batched_xs<1, 8, F>,
-                        (const void*)moe::moe_gate_up_3d_batched_xs<2, 8, F>,
-                        (const void*)moe::moe_gate_up_3d_batched_xs<4, 8, F>,
-                        (const void*)moe::moe_gate_up_3d_batched_xs<8, 8, F>,
-                        (const void*)moe::moe_gate_up_3d_batched_xs<1, 32, F>,
-                        (const void*)moe::moe_gate_up_3d_batched_xs<2, 32, F>,
-                        (const void*)moe::moe_gate_up_3d_batched_xs<4, 32, F>,
-                        (const void*)moe::moe_gate_up_3d_batched_xs<8, 32, F>})
+  for (const void* f : {(const void*)moe::moe_gate_up_3d_batched_xs<1, 8, F, 1>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<2, 8, F, 1>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<4, 8, F, 1>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<8, 8, F, 1>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<2, 8, F, 2>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<1, 32, F, 1>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<2, 32, F, 1>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<4, 32, F, 1>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<8, 32, F, 1>,
+                        (const void*)moe::moe_gate_up_3d_batched_xs<2, 32, F, 2>})
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   return e;

@@ -342,7 +342,8 @@ __host__ __device__ constexpr size_t gate_up_xs_smem(int T, int H) {
   return (size_t)kXsWarps * 32 * 4 + (size_t)T * (H >> 5) * (64 + 4);
 }
 
-template <int NT, int KMAX, class F>
+// D: weight blocks per lane in flight (1, or 2 when registers allow).
+template <int NT, int KMAX, class F, int D = 1>
 __global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_3d_batched_xs(GateUpParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
@@ -408,36 +409,46 @@ __global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_3d_batched_xs(GateU
       float ag[NT], au[NT];
 #pragma unroll
       for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
-      // the next block's codes are in flight while this one is applied
-      uint32_t qg[F::kWords], qu[F::kWords];
-      uint32_t s_g = 0, s_u = 0;
-      int b = lane;
-      if (b < nb) {
-        F::load(wg + b * CB, qg);
-        F::load(wu + b * CB, qu);
-        s_g = ld_scale(sg + b);
-        s_u = ld_scale(su + b);
+      // the next D blocks' codes are in flight while one is applied
+      uint32_t qg[D][F::kWords], qu[D][F::kWords];
+      uint32_t s_g[D], s_u[D];
+#pragma unroll
+      for (int d = 0; d < D; ++d) {
+        const int b = lane + 32 * d;
+        s_g[d] = s_u[d] = 0;
+        if (b < nb) {
+          F::load(wg + b * CB, qg[d]);
+          F::load(wu + b * CB, qu[d]);
+          s_g[d] = ld_scale(sg + b);
+          s_u[d] = ld_scale(su + b);
+        }
       }
 #pragma unroll 1
-      for (; b < nb; b += 32) {
-        uint32_t whg[16], whu[16];
-        F::decode(qg, swap, whg);
-        F::decode(qu, swap, whu);
-        const float scg = ue8m0_to_f32(s_g), scu = ue8m0_to_f32(s_u);
-        if (b + 32 < nb) {
-          F::load(wg + (b + 32) * CB, qg);
-          F::load(wu + (b + 32) * CB, qu);
-          s_g = ld_scale(sg + b + 32);
-          s_u = ld_scale(su + b + 32);
-        }
+      for (int b0 = lane; b0 < nb; b0 += 32 * D) {
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          if (n < nt) {
-            const int xb = tok[n] * nb + b;
-            const uint8_t* act = xs + 64 * xb;
-            const float fx = xf[xb];
-            ag[n] = fmaf(dot_block_h(whg, act, lb) * fx, scg, ag[n]);
-            au[n] = fmaf(dot_block_h(whu, act, lb) * fx, scu, au[n]);
+        for (int d = 0; d < D; ++d) {
+          const int b = b0 + 32 * d;
+          if (b < nb) {
+            uint32_t whg[16], whu[16];
+            F::decode(qg[d], swap, whg);
+            F::decode(qu[d], swap, whu);
+            const float scg = ue8m0_to_f32(s_g[d]), scu = ue8m0_to_f32(s_u[d]);
+            if (b + 32 * D < nb) {
+              F::load(wg + (b + 32 * D) * CB, qg[d]);
+              F::load(wu + (b + 32 * D) * CB, qu[d]);
+              s_g[d] = ld_scale(sg + b + 32 * D);
+              s_u[d] = ld_scale(su + b + 32 * D);
+            }
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              if (n < nt) {
+                const int xb = tok[n] * nb + b;
+                const uint8_t* act = xs + 64 * xb;
+                const float fx = xf[xb];
+                ag[n] = fmaf(dot_block_h(whg, act, lb) * fx, scg, ag[n]);
+                au[n] = fmaf(dot_block_h(whu, act, lb) * fx, scu, au[n]);
+              }
+            }
           }
         }
       }
