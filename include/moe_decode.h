@@ -137,10 +137,15 @@ moe_status_t moe_dedup_schedule(moe_decode_t handle, int32_t T, const int32_t* t
                                 int32_t* n_uniq, void* stream);
 
 /*
- * Gate/up projection (kernel moe_gate_up_3d_batched; the warp-decode post,
- * "How the two kernels work", first two paragraphs). Each unique expert's
- * gate and up rows are streamed once per group of tokens and serve every
- * token routed to it.
+ * Gate/up projection (the warp-decode post, "How the two kernels work", first
+ * two paragraphs). Each unique expert's gate and up rows are streamed once
+ * per group of tokens and serve every token routed to it. The kernel depends
+ * on T and the shape (moe_decode_kernel_name reports it):
+ * moe_gate_up_3d_batched (x read through L1), moe_gate_up_3d_batched_xs (x
+ * staged in shared memory as power-of-two-scaled f16 blocks), or, from 16
+ * tokens, moe_gate_up_tma (16-neuron weight tiles streamed by TMA into a
+ * shared-memory ring, products on mma.sync with FP32 accumulation). Groups
+ * are at most 32 tokens, fewer when that lets x fit in shared memory.
  *   x         device bf16 [T, H]     32-byte aligned
  *   topk_ids  device int32 [T, k]
  *   h         device bf16 [T, k, I]  out, 32-byte aligned
@@ -149,9 +154,13 @@ moe_status_t moe_gate_up(moe_decode_t handle, int32_t T, const uint16_t* x,
                          const int32_t* topk_ids, uint16_t* h, void* stream);
 
 /*
- * Down projection with the routing-weighted sum over the top-k experts
- * (kernel moe_down_3d_batched; the warp-decode post, "How the two kernels
- * work", third paragraph onward). One warp owns one output y[t, r].
+ * Down projection with the routing-weighted sum over the top-k experts (the
+ * warp-decode post, "How the two kernels work", third paragraph onward).
+ * Kernel by T and shape: moe_down_3d_batched (one warp per output y[t, r]),
+ * from 2 tokens moe_down_tma (a 16-row tile of y[t] per item, each distinct
+ * routed expert's rows streamed by TMA, one warp per row), from 16 tokens
+ * moe_down_mma (one CTA per 16-row tile of y for every token, each unique
+ * expert's rows streamed once, products on mma.sync); no atomics in any.
  *   h         device bf16 [T, k, I]  32-byte aligned
  *   topk_ids  device int32 [T, k]
  *   topk_w    device float [T, k]
