@@ -13,7 +13,7 @@ Source: the warp-decode post (cursor.com/blog/warp-decode).
       intermediate activations.
   "Improved accuracy": activations stay BF16 and accumulators FP32.
 
-Readings where the pages are silent (each is also listed in the design doc):
+Readings where the pages are silent:
 
   * W_gateup[e] is [2I, H]: rows [0, I) gate, rows [I, 2I) up.
   * SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)).
