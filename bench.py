@@ -208,8 +208,12 @@ def run_reference(args, rank, world):
     seed = wl.seed_of(args.workload)
     if rank != 0:
         return
-    # the oracle needs only the routed experts; generate them lazily
+    # every expert generated before the timed steps when they fit in host
+    # memory (the steps then time the oracle alone); else only the routed
+    # ones, as they are first used
     cache = {}
+    if w.E * w.weight_bytes(args.format) <= 4e9:
+        cache = wl.make_experts(w, seed, range(w.E), fmt=args.format)
 
     def experts(e):
         if e not in cache:
