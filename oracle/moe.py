@@ -50,11 +50,18 @@ def _get(experts: ExpertSource, e: int):
 
 # Weight formats: MXFP8 (E4M3 codes, one byte each) and MXFP4 (E2M1 codes,
 # two to a byte); both carry one UE8M0 scale per 32 elements along K.
+def _float_weights(w, scales):
+    """fmt "float": the expert holds full-precision weights (scales unused)."""
+    return np.asarray(w, dtype=np.float64)
+
+
 def _dq(fmt: str):
     if fmt == "mxfp8":
         return dequantize
     if fmt == "mxfp4":
         return dequantize_mxfp4
+    if fmt == "float":
+        return _float_weights
     raise ValueError(f"unknown weight format {fmt!r}")
 
 
@@ -170,7 +177,7 @@ def down(h: np.ndarray, ids: np.ndarray, w: np.ndarray, experts: ExpertSource, E
     terms = np.zeros((T, k, len(rows)), dtype=np.float64)
     for e, slots in _slots_by_expert(ids, E, tokens).items():
         wd, sd = _get(experts, e)[2:4]
-        W = dequantize(wd[rows], sd[rows])
+        W = dequantize(wd[rows], None if sd is None else sd[rows])
         for t, j in slots:
             terms[t, j] = wt[t, j] * (W @ h[t, j])
         del W

@@ -55,6 +55,7 @@ import torch
 __all__ = [
     "Workload", "WORKLOADS", "workload", "seed_of",
     "make_x", "make_logits", "encode_mxfp8", "encode_mxfp4", "make_expert", "make_experts",
+    "make_expert_float",
     "FORMATS",
     "bf16_bits_to_f64", "NAN_CODE",
 ]
@@ -182,6 +183,17 @@ def encode_mxfp4(w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
 
 
 FORMATS = {"mxfp8": encode_mxfp8, "mxfp4": encode_mxfp4}
+
+
+def make_expert_float(w: Workload, seed: int, e: int):
+    """One expert's weights as drawn, before any encoding: (W_gateup float32
+    [2I, H], None, W_down float32 [H, I], None) (the full-precision weights the
+    encoded ones approximate)."""
+    gu = _rng(seed, 3, e).standard_normal((2 * w.I, w.H), dtype=np.float32)
+    gu *= np.float32(w.sigma)
+    dn = _rng(seed, 4, e).standard_normal((w.H, w.I), dtype=np.float32)
+    dn *= np.float32(w.sigma)
+    return gu, None, dn, None
 
 
 def make_expert(w: Workload, seed: int, e: int, fmt: str = "mxfp8"):
