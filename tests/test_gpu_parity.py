@@ -139,3 +139,26 @@ def _check_schedule(dev, E, k, ids):
     assert np.array_equal(pairs.cpu().numpy()[:len(p_ref)], p_ref)
     bad = bool(((ids < 0) | (ids >= E)).any())
     assert layer.get_error() == (1 if bad else 0)
+
+
+def test_gpu_output_closer_than_classic_path(dev):
+    # the post's accuracy claim on the product path: the library's bf16 y
+    # against the layer on the full-precision weights the MXFP8 codes were
+    # encoded from, compared with the classic path's (h requantised to MXFP8)
+    case = Case(1)
+    w = case.w
+    layer = _layer(case, dev)
+    x = bf16_tensor(case.x_bits, dev)
+    ids = torch.from_numpy(case.ids).to(dev)
+    tw = torch.from_numpy(case.tw).to(dev)
+    y = tensor_to_f64(layer.layer(x, ids, tw))
+    layer.close()
+    exf = {e: wl.make_expert_float(w, case.seed, e) for e in case.experts}
+    ref = oracle.layer(case.x64(), case.ids, case.tw, exf, w.E, w.H, w.I, fmt="float")["y_pure"]
+    yc = oracle.bf16_rne(oracle.layer_classic(case.x64(), case.ids, case.tw, case.experts,
+                                              w.E, w.H, w.I))
+    e_gpu = np.linalg.norm(y - ref) / np.linalg.norm(ref)
+    e_classic = np.linalg.norm(yc - ref) / np.linalg.norm(ref)
+    print(f"vs full-precision weights: GPU {e_gpu:.4e}, classic path {e_classic:.4e}, "
+          f"ratio {e_classic / e_gpu:.3f}")
+    assert e_classic > 1.05 * e_gpu
