@@ -241,6 +241,33 @@ int32_t moe_decode_fused_layer(moe_decode_t handle);
 const char* moe_decode_kernel_name(moe_decode_t handle, int32_t T, int32_t which);
 
 /*
+ * Test support: the launch plan the library would make, computed on the host
+ * alone (no device, no allocation) for a configuration, a device with
+ * num_sms SMs and smem_per_block bytes of opt-in shared memory per CTA, and
+ * calls of T tokens. The weight pointers are taken as suitably aligned.
+ *   fused*        the one-launch single-token layer: whether it fits, its
+ *                 K-chunk (weights per row per stage), ring slots and slot
+ *                 bytes, down rows per chunk and chunks per slot, and its
+ *                 dynamic shared memory
+ *   gate_up_*     tokens per gate/up launch, its kernel (0 reads x through
+ *                 L1, 1 stages x, 2 TMA ring with mma.sync), ring slots (0
+ *                 without a ring) and dynamic shared memory
+ *   down_*        down kernel for min(T, 32) tokens (0 one warp per output,
+ *                 1 TMA ring token by token, 2 TMA ring with mma.sync), ring
+ *                 slots and dynamic shared memory
+ * Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED_SHAPE as
+ * moe_decode_create would for the configuration.
+ */
+typedef struct {
+  int32_t fused, fused_kc, fused_slots, fused_slot_bytes, fused_down_rows, fused_down_per_slot,
+      fused_smem;
+  int32_t gate_up_group, gate_up_kernel, gate_up_slots, gate_up_smem;
+  int32_t down_kernel, down_slots, down_smem;
+} moe_decode_plan_t;
+moe_status_t moe_decode_plan(const moe_decode_config_t* cfg, int32_t num_sms,
+                             int32_t smem_per_block, int32_t T, moe_decode_plan_t* out);
+
+/*
  * Test support for failure detection (the pages have no counterpart): moves
  * this handle's launch counter far ahead of its grid-barrier counter, so that
  * the next one-launch call's grid barrier can never be met. Every CTA's

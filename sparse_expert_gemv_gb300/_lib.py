@@ -42,6 +42,14 @@ class MoEError(RuntimeError):
                          STATUS_NAMES.get(status, str(status)))
 
 
+class MoEPlan(ctypes.Structure):
+    """moe_decode_plan_t: the launch plan moe_decode_plan reports."""
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "fused", "fused_kc", "fused_slots", "fused_slot_bytes", "fused_down_rows",
+        "fused_down_per_slot", "fused_smem", "gate_up_group", "gate_up_kernel", "gate_up_slots",
+        "gate_up_smem", "down_kernel", "down_slots", "down_smem")]
+
+
 _p = ctypes.c_void_p
 _i32 = ctypes.c_int32
 _st = ctypes.c_int
@@ -61,6 +69,7 @@ SIGNATURES = {
     "moe_decode_version": (_i32, []),
     "moe_decode_fused_layer": (_i32, [_p]),
     "moe_decode_kernel_name": (ctypes.c_char_p, [_p, _i32, _i32]),
+    "moe_decode_plan": (_st, [ctypes.POINTER(MoEConfig), _i32, _i32, _i32, ctypes.POINTER(MoEPlan)]),
     "moe_decode_arm_barrier_timeout": (_st, [_p]),
     "moe_decode_layer_noalloc": (_st, [ctypes.POINTER(MoEConfig), _p, _p, _p, _p, _i32, _p, _p, _p,
                                        _p, _p]),

@@ -528,10 +528,14 @@ bool encode_fused_maps(moe_decode* m, int KC, int RC) {
 // the 128-byte swizzle, its scales as [E*2I][H/128] uint32 with boxes of 16
 // rows x KC/32 scale bytes. False when the shape or the scale pointer does
 // not suit them.
+bool gu_tma_shape_ok(const moe_decode* m) {
+  return m->cfg.H % gu_tma_kc(m) == 0 && aligned(m->sgu, 16);
+}
+
 bool encode_gu_tma_maps(moe_decode* m) {
   const moe_decode_config_t& c = m->cfg;
   const int KC = gu_tma_kc(m);
-  if (c.H % KC || !aligned(m->sgu, 16)) return false;
+  if (!gu_tma_shape_ok(m)) return false;
   const int RB = c.H / 32 * code_bytes_per_block(m);
   const uint64_t rows = (uint64_t)c.E * 2 * c.I;
   return encode_u32_3d(&m->tm_gu_codes, m->wgu, 32, RB / 128, rows, RB, 1, moe::kGuRows,
@@ -545,9 +549,13 @@ bool encode_gu_tma_maps(moe_decode* m) {
 // scales as [E][H*I/128] uint32 with boxes of 16 rows' scale bytes. False
 // when the shape or the pointers do not suit them (I a multiple of 128 and at
 // most 2048, scale array 16-byte aligned).
+bool dn_tma_shape_ok(const moe_decode* m) {
+  return m->cfg.I % 128 == 0 && m->cfg.I <= 2048 && aligned(m->sd, 16);
+}
+
 bool encode_dn_tma_maps(moe_decode* m) {
   const moe_decode_config_t& c = m->cfg;
-  if (c.I % 128 || c.I > 2048 || !aligned(m->sd, 16)) return false;
+  if (!dn_tma_shape_ok(m)) return false;
   const int IB = c.I / 32 * code_bytes_per_block(m);
   const int kin = std::min(256, IB / 4);
   return encode_u32_4d(&m->tm_dn_codes, m->wd, kin, IB / (4 * kin), c.H, c.E, moe::kDnRows) &&
@@ -979,6 +987,52 @@ const char* moe_status_string(moe_status_t status) {
 int32_t moe_decode_version(void) { return kVersion; }
 
 int32_t moe_decode_fused_layer(moe_decode_t m) { return m ? (m->fused_ok ? 1 : 0) : -1; }
+
+moe_status_t moe_decode_plan(const moe_decode_config_t* cfg, int32_t num_sms,
+                             int32_t smem_per_block, int32_t T, moe_decode_plan_t* out) {
+  if (!cfg || !out || num_sms < 1 || smem_per_block < 1 || T < 1) return MOE_ERR_INVALID_ARG;
+  const moe_decode_config_t c = *cfg;
+  if (c.E < 1 || c.k < 1 || c.H < 1 || c.I < 1 || c.k > c.E) return MOE_ERR_INVALID_ARG;
+  if (c.E > kMaxE || c.k > kMaxK || c.H % 32 || c.I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((c.flags & ~kKnownFlags) != 0) return MOE_ERR_INVALID_ARG;
+  // a handle on the stack with 256-byte aligned stand-in weight pointers
+  // (never dereferenced) and the given device limits
+  moe_decode m = {};
+  m.cfg = c;
+  m.wgu = m.sgu = m.wd = m.sd = reinterpret_cast<const uint8_t*>(uintptr_t{256});
+  m.num_sms = num_sms;
+  m.smem_per_block = (size_t)smem_per_block;
+  m.fused_ok = true;
+  m.gu_tma_ok = gu_tma_shape_ok(&m);
+  m.dn_tma_ok = dn_tma_shape_ok(&m);
+  *out = moe_decode_plan_t{};
+  moe::FusedParams fp = {};
+  size_t smem = 0;
+  if (plan_fused(&m, fp, smem)) {
+    out->fused = 1;
+    out->fused_kc = fp.KC;
+    out->fused_slots = fp.SG;
+    out->fused_slot_bytes = fp.slot_g;
+    out->fused_down_rows = fp.RC;
+    out->fused_down_per_slot = fp.SR;
+    out->fused_smem = (int32_t)smem;
+  }
+  const int G = gate_up_group(&m, T);
+  int SG = 0;
+  smem = 0;
+  out->gate_up_group = G;
+  const GuKind gk = gate_up_kind(&m, G, SG, smem);
+  out->gate_up_kernel = gk == GuKind::kL1 ? 0 : gk == GuKind::kXs ? 1 : 2;
+  out->gate_up_slots = gk == GuKind::kTma ? SG : 0;
+  out->gate_up_smem = gk == GuKind::kL1 ? 0 : (int32_t)smem;
+  SG = 0;
+  smem = 0;
+  const DnKind dk = down_kind(&m, std::min<int>(T, moe::kMaxTokensPerLaunch), SG, smem);
+  out->down_kernel = dk == DnKind::kWarp ? 0 : dk == DnKind::kTma ? 1 : 2;
+  out->down_slots = dk == DnKind::kWarp ? 0 : SG;
+  out->down_smem = (int32_t)smem;
+  return MOE_OK;
+}
 
 const char* moe_decode_kernel_name(moe_decode_t m, int32_t T, int32_t which) {
   if (!m || T <= 0 || (which != 0 && which != 1)) return "";
