@@ -47,3 +47,23 @@ def test_two_gloo_ranks_agree_on_the_slowest_time():
         assert w == 2
         assert t_job == pytest.approx(1.5)
         assert value == pytest.approx(42 / 1.5)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    # the bench's reference arm launched as the driver launches it at N > 1
+    # (torchrun, one process per rank; gloo here): rank 0 alone runs the
+    # oracle and prints one JSON line, the other rank exits 0 without work
+    import json
+    import subprocess
+    port = _free_port()
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1", "--workload", "0"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
