@@ -151,3 +151,37 @@ def test_make_expert_mxfp4_shapes_and_bytes():
     assert wd.shape == (w.H, w.I // 2) and sd.shape == (w.H, w.I // 32)
     assert w.weight_bytes("mxfp4") == wgu.size + sgu.size + wd.size + sd.size
     assert w.weight_bytes("mxfp8") == w.weight_bytes_per_expert
+
+
+def _scalar_loop_agrees(dq):
+    rng = np.random.default_rng(11)
+    packed = rng.integers(0, 256, size=(2, 64), dtype=np.uint8)
+    scales = rng.integers(110, 140, size=(2, 4), dtype=np.uint8)
+    got = dq(packed, scales)
+    for r in range(2):
+        for i in range(128):
+            byte = int(packed[r, i // 2])
+            code = (byte >> 4) if i % 2 else (byte & 0xF)
+            if got[r, i] != oracle.e2m1_decode(code) * 2.0 ** (int(scales[r, i // 32]) - 127):
+                return False
+    return True
+
+
+def test_pins_catch_planted_mxfp4_mistakes():
+    # a swapped nibble order and a scale indexed per packed byte, planted in
+    # copies of the oracle's decode, must each fail the scalar-loop pin
+    assert _scalar_loop_agrees(mxfp4.dequantize)
+
+    def swapped(packed, scales):
+        p = np.asarray(packed, dtype=np.uint8)
+        return mxfp4.dequantize(((p & 0xF) << 4) | (p >> 4), scales)
+
+    def scale_per_byte(packed, scales):
+        codes = mxfp4.unpack(packed)
+        K = codes.shape[-1]
+        s = np.asarray(scales, dtype=np.uint8)
+        idx = np.minimum(np.arange(K) // 2 // 32 * 2, s.shape[-1] - 1)   # K/2 bytes per 32 * 2
+        return oracle.E2M1[codes] * oracle.UE8M0[s[..., idx]]
+
+    assert not _scalar_loop_agrees(swapped)
+    assert not _scalar_loop_agrees(scale_per_byte)
