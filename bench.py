@@ -7,15 +7,20 @@ of T tokens of the batch-1 decode workload (E=128, k=8, H=2048, I=768, T=1,
 MXFP8 weights, seeded synthetic data). Steps rotate over L resident copies of
 the layer at distinct device addresses with fresh routing and activations per
 step, so the footprint (L x 604 MB) is far larger than L2 and every step streams
-its weights from HBM. The K timed steps are one CUDA-graph replay bracketed by
-CUDA events on the replay stream.
+its weights from HBM. The K timed steps are one CUDA graph; it is replayed R
+times (--replays), each replay bracketed by CUDA events on the replay stream,
+and the line reports the median replay (p10 and p90 beside it). A cold single
+layer is timed too: a one-step graph replayed after an L2 flush that stays
+outside the event pair.
 
 Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs an
 independent replica of the same workload ("replicas only": the layer has no
 exchange step on one GPU); value = all ranks' tokens / the slowest rank's time.
 
 --impl reference times the CPU oracle (float64 numpy) on the host cores on a
-bounded sample of the same workload.
+bounded sample of the same workload. Our arm's cpu_baseline times the same
+oracle on one host thread and on every core of the process's affinity set
+(one forked worker per core, before any CUDA call), with the CPU model.
 
 --workload N runs one of the other configurations instead (0: tiny, 2: T=8,
 3: Zipf-skewed T=32, 4: large experts T=16), for reports; the default line is
@@ -27,7 +32,9 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import multiprocessing
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -59,7 +66,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=LAYERS)
-    ap.add_argument("--cpu-sample-s", type=float, default=12.0)
+    ap.add_argument("--cpu-sample-s", type=float, default=10.0)
+    ap.add_argument("--replays", type=int, default=30)
+    ap.add_argument("--cold", type=int, default=100, help="timed cold single-layer replays")
     # the other configurations, for reports (the default line is workload 1)
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--format", default="mxfp8", choices=sorted(wl.FORMATS))
@@ -203,6 +212,58 @@ def cpu_oracle_rate(w, seed, experts, budget_s, fmt="mxfp8"):
     return w.T * n / dt, n, dt
 
 
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
+# experts of the all-cores CPU sample, set before the pool forks (the workers
+# inherit them instead of regenerating them)
+_FORK_STATE = {}
+
+
+def _cpu_worker(step0):
+    st = _FORK_STATE
+    w, seed, experts, budget, fmt = st["w"], st["seed"], st["experts"], st["budget"], st["fmt"]
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < budget or n < 2:
+        oracle_steps(w, seed, experts, 1, step0=step0 + n, fmt=fmt)
+        n += 1
+    return n
+
+
+def cpu_oracle_rate_all_cores(w, seed, experts, budget_s, fmt="mxfp8"):
+    """tokens/s of the oracle on every core of the affinity set: one forked
+    worker per core, each running single-threaded steps for ~budget_s. Call
+    before any CUDA call (the workers are forked)."""
+    cores = len(os.sched_getaffinity(0))
+    _FORK_STATE.update(w=w, seed=seed, experts=experts, budget=budget_s, fmt=fmt)
+    ctx = multiprocessing.get_context("fork")
+    with ctx.Pool(cores) as pool:
+        t0 = time.perf_counter()
+        counts = pool.map(_cpu_worker, [50_000 + 10_000 * i for i in range(cores)])
+        wall = time.perf_counter() - t0
+    _FORK_STATE.clear()
+    return w.T * sum(counts) / wall, cores, sum(counts), wall
+
+
+def cpu_baseline(w, seed, experts, budget_s, fmt):
+    r1, n1, dt1 = cpu_oracle_rate(w, seed, experts, budget_s, fmt=fmt)
+    ra, cores, na, dta = cpu_oracle_rate_all_cores(w, seed, experts, budget_s, fmt=fmt)
+    return {"value": r1, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n1} decode steps of the workload (T={w.T}, fresh routing each), "
+                      f"{dt1:.1f} s of float64 numpy on one host thread; all cores: {na} steps "
+                      f"in {dta:.1f} s over {cores} forked single-threaded workers",
+            "cores_all": cores, "value_all": ra, "cpu_model": cpu_model()}
+
+
 def run_reference(args, rank, world):
     w = wl.workload(args.workload)
     seed = wl.seed_of(args.workload)
@@ -243,22 +304,30 @@ def run_reference(args, rank, world):
 # ---------------------------------------------------------------------------
 
 def run_ours(args, rank, world, local):
-    from sparse_expert_gemv_gb300 import MoEDecode
-
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
     w = wl.workload(args.workload)
     seed = wl.seed_of(args.workload)
     K, W, L = args.steps, args.warmup, args.layers
     T, E, k, H, I = w.T, w.E, w.k, w.H, w.I
-
-    # one layer's weights, L resident copies at distinct addresses; a layer of
-    # several GB (workload 4) gets random code bytes generated on the device
-    # instead (the timing does not depend on the values; no oracle leg)
     fmt = args.format
     per = 2 if fmt == "mxfp4" else 1              # elements per code byte
     expert_bytes = w.weight_bytes(fmt)
     big = w.E * expert_bytes > 4e9
+    experts = None if big else wl.make_experts(w, seed, range(E), fmt=fmt)
+
+    # the CPU oracle baseline first: its all-cores leg forks workers, which
+    # must happen before this process makes any CUDA call
+    cpu = None
+    if rank == 0 and world == 1 and experts is not None:
+        cpu = cpu_baseline(w, seed, experts, args.cpu_sample_s, fmt)
+
+    from sparse_expert_gemv_gb300 import MoEDecode
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    # one layer's weights, L resident copies at distinct addresses; a layer of
+    # several GB (workload 4) gets random code bytes generated on the device
+    # instead (the timing does not depend on the values; no oracle leg)
     if big:
         L = min(L, 2)
         gen = torch.Generator(device=dev)
@@ -271,11 +340,9 @@ def run_ours(args, rank, world, local):
         def scales(*shape):
             return torch.randint(118, 124, shape, dtype=torch.uint8, device=dev, generator=gen)
 
-        experts = None
         base = [codes(E, 2 * I, H // per), scales(E, 2 * I, H // 32), codes(E, H, I // per),
                 scales(E, H, I // 32)]
     else:
-        experts = wl.make_experts(w, seed, range(E), fmt=fmt)
         host = [np.stack([experts[e][i] for e in range(E)]) for i in range(4)]
         base = [torch.from_numpy(a).to(dev) for a in host]
     layers = []
@@ -335,6 +402,12 @@ def run_ours(args, rank, world, local):
     g_gu = None if fused else capture(range(W, W + K), only_gate_up=True)
     stream = torch.cuda.current_stream()
 
+    # a cold single layer: one step of the first layer copy, replayed after an
+    # L2 flush (a write of twice the L2 size) that stays outside the event pair
+    g_cold = capture([W])
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+
     def timed(g):
         barrier(world)
         torch.cuda.synchronize()
@@ -347,6 +420,20 @@ def run_ours(args, rank, world, local):
         barrier(world)
         return e0.elapsed_time(e1) * 1e-3
 
+    def timed_cold(n):
+        out = []
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        for _ in range(n):
+            flush.fill_(1.0)
+            e0.record(stream)
+            g_cold.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1) * 1e-3)
+        return out
+
+    R = max(1, args.replays)
     with ClockSampler(dev) as clk:
         g_warm.replay()
         torch.cuda.synchronize()
@@ -355,10 +442,27 @@ def run_ours(args, rank, world, local):
         while time.perf_counter() < t_end:
             g_main.replay()
             torch.cuda.synchronize()
-        dt = timed(g_main)
-        dt_gu = None if fused else timed(g_gu)
+        # R replays of the K-step graph, each bracketed by a barrier and a
+        # synchronize; the line reports the median replay
+        dts = [timed(g_main) for _ in range(R)]
+        dt_gus = None if fused else [timed(g_gu) for _ in range(max(3, R // 3))]
+        timed_cold(10)
+        colds = timed_cold(max(1, args.cold))
     clocks = clk.summary()
+    dt = statistics.median(dts)
+    dt_gu = None if fused else statistics.median(dt_gus)
     dt_max = reduce_max(dt, world)
+    per_step = np.array(dts) / K * 1e6
+    spread = {"replays": R, "median_us": float(np.median(per_step)),
+              "p10_us": float(np.percentile(per_step, 10)),
+              "p90_us": float(np.percentile(per_step, 90)),
+              "min_us": float(per_step.min()), "max_us": float(per_step.max())}
+    cold_us = np.array(colds) * 1e6
+    cold = {"replays": len(colds), "warmup": 10, "median_us": float(np.median(cold_us)),
+            "p10_us": float(np.percentile(cold_us, 10)),
+            "p90_us": float(np.percentile(cold_us, 90)),
+            "l2_flush_bytes": int(flush.numel() * 4)}
+    del flush
 
     tokens = T * K * world
     value = tokens / dt_max
@@ -400,12 +504,6 @@ def run_ours(args, rank, world, local):
     # the same outputs through both paths
     ref_ok = torch.equal(yh.view(torch.int16), y[W + K - 1].cpu().view(torch.int16))
 
-    cpu = None
-    if rank == 0 and world == 1 and experts is not None:
-        r, n, cdt = cpu_oracle_rate(w, seed, experts, args.cpu_sample_s, fmt=fmt)
-        cpu = {"value": r, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} decode steps of the workload (T={T}, fresh routing each), "
-                         f"{cdt:.1f} s of float64 numpy on one host thread"}
 
     for _, lay in layers:
         lay.close()
@@ -424,10 +522,16 @@ def run_ours(args, rank, world, local):
                 "l2": f"inputs larger than L2: {L} resident layer copies "
                       f"({L * w.E * expert_bytes / 1e9:.1f} GB) with fresh routing "
                       "and activations every step",
-                "timing": "one CUDA-graph replay of K steps, CUDA events on the replay stream",
+                "timing": f"median of {R} replays of a K-step CUDA graph, each bracketed by "
+                          "CUDA events on the replay stream (barrier + synchronize around each)",
                 "parallelism": f"replicas x{world}",
             },
             "hbm_gbs": hbm_gbs,
+            "step_us": spread,
+            "p10_us": spread["p10_us"],
+            "p90_us": spread["p90_us"],
+            "cold_single_layer_us": cold["median_us"],
+            "cold_single_layer": cold,
             "weight_bytes_per_step": float(bytes_step[W:].mean()),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,

@@ -97,7 +97,8 @@ typedef struct moe_decode* moe_decode_t;
  * no alignment (16-byte aligned scale arrays enable the one-launch
  * single-token layer, which with MXFP4 also needs H a multiple of 1024). Allocates 32 bytes of device
  * state (the error word and the one-launch kernel's launch and grid-barrier
- * counters) and, when max_T > 0, the staging buffers of
+ * counters), one CUDA event and one non-blocking stream (for
+ * moe_decode_get_error) and, when max_T > 0, the staging buffers of
  * moe_decode_forward_host. *out receives the handle; on error *out is NULL.
  */
 moe_status_t moe_decode_create(const moe_decode_config_t* cfg,
@@ -207,11 +208,21 @@ moe_status_t moe_decode_forward_host(moe_decode_t handle, int32_t T, const uint1
                                      uint16_t* y_host, void* stream);
 
 /*
- * Wait for the device, read and clear the device error word. *device_flags
- * receives the MOE_DEVICE_* bits seen since the last call; the return value
- * is MOE_ERR_DEVICE_FAULT when any bit was set, MOE_OK otherwise.
+ * Read and clear the handle's device error word. *device_flags receives the
+ * MOE_DEVICE_* bits latched since the last read; the return value is
+ * MOE_ERR_DEVICE_FAULT when any bit was set, MOE_OK otherwise.
+ * moe_decode_get_error first waits for the work of this handle's most recent
+ * call that was not being captured into a CUDA graph (an event the handle
+ * records after each call's launches), and for nothing else: kernels of other
+ * streams and other libraries keep running. The read and the clear run on a
+ * private non-blocking stream of the handle. Errors of earlier calls made on
+ * another stream may still be in flight then; after replaying a graph, or to
+ * cover every call made on one stream, use moe_decode_get_error_stream, which
+ * waits for `stream` (a cudaStream_t) instead.
  */
 moe_status_t moe_decode_get_error(moe_decode_t handle, uint32_t* device_flags);
+moe_status_t moe_decode_get_error_stream(moe_decode_t handle, void* stream,
+                                         uint32_t* device_flags);
 
 /* Static, human-readable name of a status. */
 const char* moe_status_string(moe_status_t status);
@@ -304,7 +315,16 @@ moe_status_t moe_decode_arm_barrier_timeout(moe_decode_t handle);
  * is written earlier in the same call), so calls whose work overlaps on the
  * GPU, for example on two streams, race and corrupt each other's h.
  * Out-of-range expert ids still contribute nothing, but this call has no way
- * to report them.
+ * to report them. Nor can it report a bounded device wait that gave up
+ * (MOE_DEVICE_TIMEOUT on a handle): with T = 1 the one-launch kernel's CTAs
+ * wait for one another on counters kept in the same array, and if such a
+ * wait runs out (for example because an overlapping call on another stream
+ * holds the SMs), that call's y is unspecified and nothing says so. Every
+ * call advances those counters by the same fixed amount whatever happens in
+ * it, so a later call that does not overlap another one is unaffected. The
+ * call plans its launches (kernel choice and TMA tensor maps) on the host and
+ * keeps the plan of the latest configuration and weight pointers per device,
+ * so repeated calls with the same layer skip that work.
  */
 #define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
 moe_status_t moe_decode_layer_noalloc(const moe_decode_config_t* cfg,

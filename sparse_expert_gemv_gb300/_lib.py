@@ -65,6 +65,7 @@ SIGNATURES = {
     "moe_decode_layer": (_st, [_p, _i32, _p, _p, _p, _p, _p, _p]),
     "moe_decode_forward_host": (_st, [_p, _i32, _p, _p, _p, _p, _p]),
     "moe_decode_get_error": (_st, [_p, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_decode_get_error_stream": (_st, [_p, _p, ctypes.POINTER(ctypes.c_uint32)]),
     "moe_status_string": (ctypes.c_char_p, [_st]),
     "moe_decode_version": (_i32, []),
     "moe_decode_fused_layer": (_i32, [_p]),

@@ -55,6 +55,12 @@ struct moe_decode {
   uint32_t* d_err;                // device error word (4 bytes) ...
   unsigned long long* d_bar;      // ... then, 8 and 16 bytes on, the fused kernel's launch
                                   // and grid-barrier counters
+  // completion of the handle's latest enqueued call (recorded outside stream
+  // capture), which moe_decode_get_error waits for, and a private
+  // non-blocking stream for reading and clearing the error word
+  cudaEvent_t done_ev;
+  bool done_recorded;
+  cudaStream_t aux;
   // staging buffers of moe_decode_forward_host (max_T tokens)
   uint16_t* d_x;
   int32_t* d_ids;
@@ -754,14 +760,79 @@ moe_status_t down_chunks(moe_decode* m, int T, const uint16_t* h, const int32_t*
   return MOE_OK;
 }
 
+// The layer's launches for T >= 1 tokens (arguments checked by the caller).
+moe_status_t layer_enqueue(moe_decode* m, int T, const uint16_t* x, const int32_t* topk_ids,
+                           const float* topk_w, uint16_t* h, uint16_t* y, cudaStream_t s) {
+  if (T == 1 && m->fused_ok) return fused_layer(m, x, topk_ids, topk_w, h, y, s);
+  moe_status_t st;
+  if (T <= moe::kMaxTokensPerLaunch) {
+    st = gate_up_chunks(m, T, x, topk_ids, h, s);
+    if (st != MOE_OK) return st;
+    return down_chunks(m, T, h, topk_ids, topk_w, y, use_pdl(m), s);
+  }
+  // several token groups: finish every gate/up launch before the downs so the
+  // early weight fetch of a down never precedes a gate/up it does not follow
+  st = gate_up_chunks(m, T, x, topk_ids, h, s);
+  if (st != MOE_OK) return st;
+  return down_chunks(m, T, h, topk_ids, topk_w, y, false, s);
+}
+
 moe_status_t check_T(const moe_decode* m, int32_t T) {
   if (!m) return MOE_ERR_INVALID_ARG;
   if (T < 0 || T > m->cfg.max_T) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
+// Host-side checks of a layer call (T = 0 passes: a no-op).
+moe_status_t check_layer(const moe_decode* m, int32_t T, const uint16_t* x, const int32_t* ids,
+                         const float* w, const uint16_t* h, const uint16_t* y) {
+  moe_status_t st = check_T(m, T);
+  if (st != MOE_OK || T == 0) return st;
+  if (!x || !ids || !w || !h || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 32) || !aligned(h, 32) || !aligned(ids, 4) || !aligned(w, 4) || !aligned(y, 2))
+    return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+// After a call has enqueued its work on s: record the handle's completion
+// event there, unless s is being captured into a graph (the event would then
+// stand for a graph node, not for work that runs).
+void mark_done(moe_decode* m, cudaStream_t s) {
+  if (!m->done_ev) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return;
+  if (cudaEventRecord(m->done_ev, s) == cudaSuccess) m->done_recorded = true;
+}
+
+moe_status_t enqueued(moe_decode* m, cudaStream_t s, moe_status_t st) {
+  if (st == MOE_OK) mark_done(m, s);
+  return st;
+}
+
+// Read and clear the device error word on the handle's private stream (and,
+// after a timeout, restart the one-launch kernel's counters from zero).
+moe_status_t read_error(moe_decode* m, uint32_t* device_flags) {
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, m->d_err, sizeof(v), cudaMemcpyDeviceToHost, m->aux) != cudaSuccess ||
+      cudaStreamSynchronize(m->aux) != cudaSuccess ||
+      cudaMemsetAsync(m->d_err, 0, sizeof(v), m->aux) != cudaSuccess ||
+      // a bounded wait that gave up may have left the launch and barrier
+      // counters out of step: start both again from zero
+      ((v & moe::kDeviceTimeout) && cudaMemsetAsync(m->d_bar, 0, 16, m->aux) != cudaSuccess) ||
+      cudaStreamSynchronize(m->aux) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *device_flags = v;
+  return v ? MOE_ERR_DEVICE_FAULT : MOE_OK;
+}
+
 void free_all(moe_decode* m) {
   if (!m) return;
+  if (m->done_ev) cudaEventDestroy(m->done_ev);
+  if (m->aux) cudaStreamDestroy(m->aux);
   cudaFree(m->d_err);
   cudaFree(m->d_x);
   cudaFree(m->d_ids);
@@ -800,7 +871,9 @@ moe_status_t moe_decode_create(const moe_decode_config_t* cfg, const uint8_t* w_
   bool ok = cudaGetDevice(&m->device) == cudaSuccess &&
             cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) ==
                 cudaSuccess &&
-            cudaMalloc(&m->d_err, 32) == cudaSuccess && cudaMemset(m->d_err, 0, 32) == cudaSuccess;
+            cudaMalloc(&m->d_err, 32) == cudaSuccess && cudaMemset(m->d_err, 0, 32) == cudaSuccess &&
+            cudaEventCreateWithFlags(&m->done_ev, cudaEventDisableTiming) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&m->aux, cudaStreamNonBlocking) == cudaSuccess;
   if (ok) m->d_bar = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(m->d_err) + 8);
   int pageable = 0;
   ok = ok && cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, m->device) ==
@@ -856,7 +929,7 @@ moe_status_t moe_route(moe_decode_t m, int32_t T, const float* logits, int32_t* 
     e = launch(moe::moe_route_topk<8>, grid, block, 0, s, use_pdl(m), logits, T, E, k, topk_ids, topk_w);
   else
     e = launch(moe::moe_route_topk<32>, grid, block, 0, s, use_pdl(m), logits, T, E, k, topk_ids, topk_w);
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return enqueued(m, s, e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA);
 }
 
 moe_status_t moe_dedup_schedule(moe_decode_t m, int32_t T, const int32_t* topk_ids, int32_t* uniq,
@@ -875,7 +948,7 @@ moe_status_t moe_dedup_schedule(moe_decode_t m, int32_t T, const int32_t* topk_i
   else
     e = launch(moe::moe_dedup_schedule_kernel<32>, dim3(1), dim3(32), 0, s, use_pdl(m), topk_ids,
                T, k, E, uniq, offsets, pairs, n_uniq, m->d_err);
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return enqueued(m, s, e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA);
 }
 
 moe_status_t moe_gate_up(moe_decode_t m, int32_t T, const uint16_t* x, const int32_t* topk_ids,
@@ -885,7 +958,8 @@ moe_status_t moe_gate_up(moe_decode_t m, int32_t T, const uint16_t* x, const int
   if (T == 0) return MOE_OK;
   if (!x || !topk_ids || !h) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 32) || !aligned(h, 32) || !aligned(topk_ids, 4)) return MOE_ERR_MISALIGNED;
-  return gate_up_chunks(m, T, x, topk_ids, h, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return enqueued(m, s, gate_up_chunks(m, T, x, topk_ids, h, s));
 }
 
 moe_status_t moe_down(moe_decode_t m, int32_t T, const uint16_t* h, const int32_t* topk_ids,
@@ -896,31 +970,17 @@ moe_status_t moe_down(moe_decode_t m, int32_t T, const uint16_t* h, const int32_
   if (!h || !topk_ids || !topk_w || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned(h, 32) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(y, 2))
     return MOE_ERR_MISALIGNED;
-  return down_chunks(m, T, h, topk_ids, topk_w, y, false, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return enqueued(m, s, down_chunks(m, T, h, topk_ids, topk_w, y, false, s));
 }
 
 moe_status_t moe_decode_layer(moe_decode_t m, int32_t T, const uint16_t* x,
                               const int32_t* topk_ids, const float* topk_w, uint16_t* h,
                               uint16_t* y, void* stream) {
-  moe_status_t st = check_T(m, T);
-  if (st != MOE_OK) return st;
-  if (T == 0) return MOE_OK;
-  if (!x || !topk_ids || !topk_w || !h || !y) return MOE_ERR_INVALID_ARG;
-  if (!aligned(x, 32) || !aligned(h, 32) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) ||
-      !aligned(y, 2))
-    return MOE_ERR_MISALIGNED;
+  moe_status_t st = check_layer(m, T, x, topk_ids, topk_w, h, y);
+  if (st != MOE_OK || T == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (T == 1 && m->fused_ok) return fused_layer(m, x, topk_ids, topk_w, h, y, s);
-  if (T <= moe::kMaxTokensPerLaunch) {
-    st = gate_up_chunks(m, T, x, topk_ids, h, s);
-    if (st != MOE_OK) return st;
-    return down_chunks(m, T, h, topk_ids, topk_w, y, use_pdl(m), s);
-  }
-  // several token groups: finish every gate/up launch before the downs so the
-  // early weight fetch of a down never precedes a gate/up it does not follow
-  st = gate_up_chunks(m, T, x, topk_ids, h, s);
-  if (st != MOE_OK) return st;
-  return down_chunks(m, T, h, topk_ids, topk_w, y, false, s);
+  return enqueued(m, s, layer_enqueue(m, T, x, topk_ids, topk_w, h, y, s));
 }
 
 moe_status_t moe_decode_forward_host(moe_decode_t m, int32_t T, const uint16_t* x_host,
@@ -942,8 +1002,13 @@ moe_status_t moe_decode_forward_host(moe_decode_t m, int32_t T, const uint16_t* 
   const void* wd = copy ? nullptr : m->host_direct ? w_host : mapped_host(w_host);
   void* yd = copy ? nullptr : m->host_direct ? y_host : const_cast<void*>(mapped_host(y_host));
   if (xd && idd && wd && yd) {
-    st = moe_decode_layer(m, T, static_cast<const uint16_t*>(xd), static_cast<const int32_t*>(idd),
-                          static_cast<const float*>(wd), m->d_h, static_cast<uint16_t*>(yd), stream);
+    // the stream is synchronised below, so no completion event is recorded
+    const uint16_t* xp = static_cast<const uint16_t*>(xd);
+    const int32_t* ip = static_cast<const int32_t*>(idd);
+    const float* wp = static_cast<const float*>(wd);
+    uint16_t* yp = static_cast<uint16_t*>(yd);
+    st = check_layer(m, T, xp, ip, wp, m->d_h, yp);
+    if (st == MOE_OK) st = layer_enqueue(m, T, xp, ip, wp, m->d_h, yp, s);
     if (st != MOE_OK) return st;
     return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
@@ -951,7 +1016,7 @@ moe_status_t moe_decode_forward_host(moe_decode_t m, int32_t T, const uint16_t* 
       cudaMemcpyAsync(m->d_ids, ids_host, (size_t)T * c.k * 4, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(m->d_w, w_host, (size_t)T * c.k * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  st = moe_decode_layer(m, T, m->d_x, m->d_ids, m->d_w, m->d_h, m->d_y, stream);
+  st = layer_enqueue(m, T, m->d_x, m->d_ids, m->d_w, m->d_h, m->d_y, s);
   if (st != MOE_OK) return st;
   if (cudaMemcpyAsync(y_host, m->d_y, (size_t)T * c.H * 2, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -960,16 +1025,16 @@ moe_status_t moe_decode_forward_host(moe_decode_t m, int32_t T, const uint16_t* 
 
 moe_status_t moe_decode_get_error(moe_decode_t m, uint32_t* device_flags) {
   if (!m || !device_flags) return MOE_ERR_INVALID_ARG;
-  uint32_t v = 0;
-  if (cudaDeviceSynchronize() != cudaSuccess ||
-      cudaMemcpy(&v, m->d_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemset(m->d_err, 0, sizeof(v)) != cudaSuccess ||
-      // a grid barrier that gave up may have left the launch and barrier
-      // counters out of step: start both again from zero
-      ((v & moe::kDeviceTimeout) && cudaMemset(m->d_bar, 0, 16) != cudaSuccess))
-    return MOE_ERR_CUDA;
-  *device_flags = v;
-  return v ? MOE_ERR_DEVICE_FAULT : MOE_OK;
+  // only the handle's own latest call is waited for: work of other streams
+  // and other libraries keeps running
+  if (m->done_recorded && cudaEventSynchronize(m->done_ev) != cudaSuccess) return MOE_ERR_CUDA;
+  return read_error(m, device_flags);
+}
+
+moe_status_t moe_decode_get_error_stream(moe_decode_t m, void* stream, uint32_t* device_flags) {
+  if (!m || !device_flags) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  return read_error(m, device_flags);
 }
 
 const char* moe_status_string(moe_status_t status) {
@@ -1091,7 +1156,11 @@ struct NoAllocDevice {
   int num_sms;
   int gate_up_ctas_per_sm;
   size_t smem_per_block;
-  bool fused_ok;
+  bool coop;          // the device supports cooperative launches
+  // the plan and tensor maps of the latest configuration and weight pointers
+  // seen on this device, reused while they stay the same
+  bool have_plan;
+  moe_decode plan;
 };
 
 std::mutex g_noalloc_mu;
@@ -1107,8 +1176,9 @@ moe_status_t noalloc_device(int dev, NoAllocDevice* out) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
       return MOE_ERR_CUDA;
-    int occ = 0;
+    int occ = 0, coop = 0;
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
         set_down_attributes() != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(
             &occ, moe::moe_gate_up_3d_batched<1, 8, moe::Mxfp8>, moe::kThreads, 0) != cudaSuccess)
@@ -1121,10 +1191,62 @@ moe_status_t noalloc_device(int dev, NoAllocDevice* out) {
     probe.cfg.k = 1;
     if (!query_fused(&probe)) return MOE_ERR_CUDA;
     d.smem_per_block = probe.smem_per_block;
+    d.coop = coop != 0;
+    d.have_plan = false;
     d.ready = true;
   }
   *out = d;
   return MOE_OK;
+}
+
+bool same_config(const moe_decode_config_t& a, const moe_decode_config_t& b) {
+  return a.E == b.E && a.k == b.k && a.H == b.H && a.I == b.I && a.flags == b.flags;
+}
+
+// The stack handle of a call: launch plan, kernel choices and tensor maps for
+// this configuration and these weights, taken from the device's cache when
+// the previous call used the same ones, else planned and cached.
+void noalloc_plan(int dev, const NoAllocDevice& d, const moe_decode_config_t& c,
+                  const uint8_t* wgu, const uint8_t* sgu, const uint8_t* wd, const uint8_t* sd,
+                  moe_decode* m) {
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    const NoAllocDevice& cached = g_noalloc_dev[dev];
+    if (cached.have_plan && same_config(cached.plan.cfg, c) && cached.plan.wgu == wgu &&
+        cached.plan.sgu == sgu && cached.plan.wd == wd && cached.plan.sd == sd) {
+      *m = cached.plan;
+      return;
+    }
+  }
+  *m = moe_decode{};
+  m->cfg = c;
+  m->wgu = wgu;
+  m->sgu = sgu;
+  m->wd = wd;
+  m->sd = sd;
+  m->device = dev;
+  m->num_sms = d.num_sms;
+  m->gate_up_ctas_per_sm = d.gate_up_ctas_per_sm;
+  m->down_smem = (size_t)c.k * c.I * sizeof(float);
+  m->smem_per_block = d.smem_per_block;
+  {
+    // the one-launch kernel: a cooperative launch whose plan depends on the shape
+    moe::FusedParams fp = {};
+    size_t smem = 0;
+    m->fused_ok = d.coop;
+    int occ = 0;
+    const void* fk = is_fp4(m) ? (const void*)moe::moe_layer_fused_t1<8, moe::Mxfp4>
+                               : (const void*)moe::moe_layer_fused_t1<8, moe::Mxfp8>;
+    m->fused_ok = m->fused_ok && plan_fused(m, fp, smem) &&
+                  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fk, moe::kFusedThreads,
+                                                                smem) == cudaSuccess &&
+                  occ >= 1 && encode_fused_maps(m, fp.KC, fp.RC);
+  }
+  m->gu_tma_ok = encode_gu_tma_maps(m);
+  m->dn_tma_ok = encode_dn_tma_maps(m);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  g_noalloc_dev[dev].plan = *m;
+  g_noalloc_dev[dev].have_plan = true;
 }
 
 }  // namespace
@@ -1151,36 +1273,12 @@ extern "C" moe_status_t moe_decode_layer_noalloc(const moe_decode_config_t* cfg,
   const moe_status_t st = noalloc_device(dev, &d);
   if (st != MOE_OK) return st;
   // a handle on the stack: every device pointer in it is either the caller's
-  // or inside the static array, and its staging buffers stay null
-  moe_decode m = {};
-  m.cfg = c;
+  // or inside the static array, and it has no staging buffers, event or stream
+  moe_decode m;
+  noalloc_plan(dev, d, c, w_gateup, s_gateup, w_down, s_down, &m);
   m.cfg.max_T = T;
-  m.wgu = w_gateup;
-  m.sgu = s_gateup;
-  m.wd = w_down;
-  m.sd = s_down;
-  m.device = dev;
-  m.num_sms = d.num_sms;
-  m.gate_up_ctas_per_sm = d.gate_up_ctas_per_sm;
-  m.down_smem = (size_t)c.k * c.I * sizeof(float);
   m.d_err = reinterpret_cast<uint32_t*>(d.scratch + kNoAllocHBytes);
   m.d_bar = reinterpret_cast<unsigned long long*>(d.scratch + kNoAllocHBytes + 8);
-  m.smem_per_block = d.smem_per_block;
-  {
-    // the fused kernel's plan depends on the call's shape
-    moe::FusedParams fp = {};
-    size_t smem = 0;
-    m.fused_ok = true;
-    int occ = 0;
-    const void* fk = is_fp4(&m) ? (const void*)moe::moe_layer_fused_t1<8, moe::Mxfp4>
-                                : (const void*)moe::moe_layer_fused_t1<8, moe::Mxfp8>;
-    m.fused_ok = plan_fused(&m, fp, smem) &&
-                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fk, moe::kFusedThreads,
-                                                               smem) == cudaSuccess &&
-                 occ >= 1 && encode_fused_maps(&m, fp.KC, fp.RC);
-  }
-  m.gu_tma_ok = encode_gu_tma_maps(&m);
-  m.dn_tma_ok = encode_dn_tma_maps(&m);
   return moe_decode_layer(&m, T, x, topk_ids, topk_w, reinterpret_cast<uint16_t*>(d.scratch), y,
                           stream);
 }

@@ -185,9 +185,14 @@ class MoEDecode:
                                           _stream(stream)), "moe_decode_forward_host")
         return y
 
-    def get_error(self) -> int:
+    def get_error(self, stream=None) -> int:
+        """Read and clear the handle's device error bits. Waits for this
+        handle's latest call, or, given a stream, for that stream."""
         flags = ctypes.c_uint32(0)
-        st = lib.moe_decode_get_error(self._h, ctypes.byref(flags))
+        if stream is None:
+            st = lib.moe_decode_get_error(self._h, ctypes.byref(flags))
+        else:
+            st = lib.moe_decode_get_error_stream(self._h, _stream(stream), ctypes.byref(flags))
         if st not in (0, 5):
             check(st, "moe_decode_get_error")
         return int(flags.value)

@@ -88,5 +88,6 @@ def test_null_handle_and_null_config(lib):
     assert lib.moe_decode_forward_host(None, 1, z, z, z, z, z) == 1
     assert lib.moe_dedup_schedule(None, 1, z, z, z, z, z, z) == 1
     assert lib.moe_decode_get_error(None, None) == 1
+    assert lib.moe_decode_get_error_stream(None, None, None) == 1
     assert lib.moe_decode_destroy(None) == 0
     assert lib.moe_decode_kernel_name(None, 1, 0) == b""

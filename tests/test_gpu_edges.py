@@ -207,6 +207,38 @@ def test_no_pdl_flag_and_host_path(dev):
         assert torch.equal(yc.view(torch.int16), want)
 
 
+def test_get_error_waits_for_its_own_work_only(dev):
+    # a long kernel on another stream keeps running while the handle's error
+    # word is read: the read waits for the handle's latest call (or a given
+    # stream), not for the whole device
+    import time
+    from sparse_expert_gemv_gb300 import MOE_DEVICE_BAD_ID
+    s = Small(dev, 8, 2, 256, 128, 1, seed=5)      # two-kernel path (no cooperative launch)
+    assert not s.layer.fused_single_token
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(3_000_000_000)            # ~1.5 s of SM clock cycles at 2 GHz
+    ids = s.ids.copy()
+    ids[0, 1] = 77                                  # out of range: latches a flag
+    x = bf16_tensor(s.x_bits, dev)
+    di = torch.from_numpy(ids).to(dev)
+    dw = torch.from_numpy(s.tw).to(dev)
+    t0 = time.perf_counter()
+    s.layer.layer(x, di, dw)
+    flags = s.layer.get_error()
+    dt = time.perf_counter() - t0
+    busy = not side.query()
+    assert flags == MOE_DEVICE_BAD_ID
+    assert busy, "the side kernel finished before the error was read; cannot tell"
+    assert dt < 0.5, f"get_error took {dt:.3f} s: it waited for another stream"
+    # the stream-scoped form waits for the given stream
+    s.layer.layer(x, di, dw)
+    assert s.layer.get_error(stream=torch.cuda.current_stream()) == MOE_DEVICE_BAD_ID
+    assert not side.query()
+    side.synchronize()
+    assert s.layer.get_error() == 0
+
+
 def test_bad_arguments_raise(dev):
     from sparse_expert_gemv_gb300 import MoEError
     s = Small(dev, 8, 2, 256, 128, 2)

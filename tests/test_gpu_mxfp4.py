@@ -61,9 +61,10 @@ def test_mxfp4_workload_parity_full(c, dev):
 
 
 def test_mxfp4_workload4_sampled_tokens(dev):
-    # E=256, H=7168, I=2048, T=16 over a full 5.9 GB MXFP4 weight set (x does
-    # not fit shared memory: the gate/up kernel reads it through L1); three
-    # tokens' experts hold real weights, every other expert NaN scales
+    # E=256, H=7168, I=2048, T=16 over a full 5.9 GB MXFP4 weight set (the 16
+    # tokens' x does not fit shared memory, so gate/up runs as two launches of
+    # 8 tokens whose x is staged); three tokens' experts hold real weights,
+    # every other expert NaN scales
     hm, ym, _ = _check_case(Case(4, tokens=[0, 7, 15], fmt="mxfp4"), dev)
     print(f"mxfp4 workload 4 (tokens 0,7,15): h {hm}  y {ym}")
 

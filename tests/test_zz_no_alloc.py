@@ -5,8 +5,9 @@ memory pool, in a plugin's enqueue function, or in a loop that must not block
 on an allocation). For them the library offers one layer call that takes no
 handle and keeps its intermediate h in static device memory. These tests call
 it through the C ABI and check it against moe_decode_layer on the same
-inputs, twice in a row (the second call finds the first call's leftovers in
-the shared array). This file sorts last so that a run stopping at the first
+inputs, several times in a row (each call finds the previous call's leftovers
+in the shared array), with several tokens (two kernels) and with one token
+(the one-launch kernel and its counters). This file sorts last so that a run stopping at the first
 failure has already run every other test.
 """
 import ctypes
@@ -56,9 +57,12 @@ def test_noalloc_layer_matches_layer_on_two_calls_in_a_row():
     experts = wl.make_experts(w, 95, range(E))
     wts = device_weights(w, experts, dev)
     ref_layer = MoEDecode(*wts, k=k, max_T=6)
+    # with one token this shape runs as the one-launch kernel, whose CTAs wait
+    # for one another on counters in the static array
+    assert ref_layer.fused_single_token
     cfg = _cfg(E, k, H, I)
     stream = torch.cuda.current_stream()
-    for call, (T, seed) in enumerate([(6, 1), (3, 2)]):
+    for call, (T, seed) in enumerate([(6, 1), (1, 3), (3, 2), (1, 4)]):
         x = bf16_tensor(wl.make_x(w, seed, T), dev)
         ids_np, tw_np = oracle.route(wl.make_logits(w, seed, T), k)
         ids = torch.from_numpy(ids_np).to(dev)
