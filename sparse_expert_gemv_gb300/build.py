@@ -13,6 +13,11 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SRC = os.path.join(HERE, "csrc", "moe_decode.cu")
 OUT = os.path.join(HERE, "libmoe_decode.so")
+# the same library with the one-launch kernel's per-CTA timeline compiled in
+# (-DMOE_TIMELINE: globaltimer stamps per CTA and phase, written to a
+# caller-supplied buffer by moe_decode_layer_timeline); never loaded by the
+# package itself
+OUT_TIMELINE = os.path.join(HERE, "libmoe_decode_timeline.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -30,18 +35,29 @@ def command(out: str = OUT, extra=()) -> list[str]:
             f"-Xlinker", f"-rpath,{cuda_lib}", *extra, SRC, "-o", out]
 
 
-def build(verbose: bool = False) -> str:
-    tmp = OUT + ".tmp"
-    cmd = command(tmp, ["-Xptxas", "-v"] if verbose else [])
+def build(verbose: bool = False, timeline: bool = False) -> str:
+    out = OUT_TIMELINE if timeline else OUT
+    tmp = out + ".tmp"
+    extra = (["-Xptxas", "-v"] if verbose else []) + (["-DMOE_TIMELINE"] if timeline else [])
+    cmd = command(tmp, extra)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("nvcc failed building libmoe_decode.so")
+        raise RuntimeError(f"nvcc failed building {os.path.basename(out)}")
     if verbose:
         sys.stderr.write(r.stderr)
-    os.replace(tmp, OUT)
-    return OUT
+    os.replace(tmp, out)
+    return out
+
+
+def stale(path: str) -> bool:
+    """True when `path` is missing or older than a CUDA source or header."""
+    if not os.path.exists(path):
+        return True
+    srcs = [os.path.join(HERE, "csrc", f) for f in os.listdir(os.path.join(HERE, "csrc"))]
+    srcs += [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))]
+    return os.path.getmtime(path) < max(os.path.getmtime(f) for f in srcs)
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    print(build(verbose="-v" in sys.argv, timeline="--timeline" in sys.argv))

@@ -2,6 +2,7 @@
 // handle lifetime, launch configuration and the programmatic-dependent-launch
 // chaining of the two projection kernels.
 #include "moe_decode.h"
+#include "moe_decode_timeline.h"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -667,7 +668,8 @@ bool query_fused(moe_decode* m) {
 }
 
 moe_status_t fused_layer(moe_decode* m, const uint16_t* x, const int32_t* ids, const float* w,
-                         uint16_t* h, uint16_t* y, cudaStream_t s) {
+                         uint16_t* h, uint16_t* y, cudaStream_t s,
+                         unsigned long long* stamps = nullptr) {
   moe::FusedParams fp = {};
   size_t smem = 0;
   plan_fused(m, fp, smem);
@@ -684,6 +686,7 @@ moe_status_t fused_layer(moe_decode* m, const uint16_t* x, const int32_t* ids, c
   fp.err = m->d_err;
   fp.launch_ctr = m->d_bar;
   fp.bar_ctr = m->d_bar + 1;
+  fp.stamps = stamps;
   fp.tm_codes = m->tm_codes;
   fp.tm_scales = m->tm_scales;
   fp.tm_dcodes = m->tm_dcodes;
@@ -1128,6 +1131,22 @@ moe_status_t moe_decode_arm_barrier_timeout(moe_decode_t m) {
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
+
+#ifdef MOE_TIMELINE
+moe_status_t moe_decode_layer_timeline(moe_decode_t m, const uint16_t* x, const int32_t* topk_ids,
+                                       const float* topk_w, uint16_t* h, uint16_t* y,
+                                       uint64_t* stamps, void* stream) {
+  moe_status_t st = check_layer(m, 1, x, topk_ids, topk_w, h, y);
+  if (st != MOE_OK) return st;
+  if (!stamps || !aligned(stamps, 8)) return MOE_ERR_INVALID_ARG;
+  if (!m->fused_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return enqueued(m, s, fused_layer(m, x, topk_ids, topk_w, h, y, s,
+                                    reinterpret_cast<unsigned long long*>(stamps)));
+}
+
+int32_t moe_decode_timeline_ctas(moe_decode_t m) { return m ? m->num_sms : -1; }
+#endif
 
 }  // extern "C"
 

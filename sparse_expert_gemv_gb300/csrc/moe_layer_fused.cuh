@@ -41,6 +41,7 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include "moe_decode_timeline.h"   // stamp indices of MOE_TIMELINE builds
 #include "moe_kernels.cuh"
 
 namespace moe {
@@ -77,6 +78,7 @@ struct FusedParams {
   uint32_t* err;
   unsigned long long* launch_ctr;  // grows by gridDim.x per launch, at kernel start
   unsigned long long* bar_ctr;     // grows by gridDim.x per launch, at the grid barrier
+  unsigned long long* stamps;      // per-CTA timeline (builds with MOE_TIMELINE), else null
   int k, E, H, I;
   int KC;       // gate/up weights per row per stage (KB = 512, 1024 or 2048 bytes), divides H
   int kin;      // uint32 words per innermost box row of tm_codes (KB/4 or 256)
@@ -269,6 +271,23 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* bar, unsigne
   return false;
 }
 
+#ifdef MOE_TIMELINE
+// Per-CTA timeline: the GPU's global nanosecond timer at the phases of
+// moe_decode_timeline.h, MOE_TL_STAMPS words per CTA.
+#define MOE_STAMP(i)                                                              \
+  do {                                                                            \
+    if (p.stamps) {                                                               \
+      unsigned long long t_;                                                      \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                      \
+      p.stamps[(size_t)blockIdx.x * MOE_TL_STAMPS + (i)] = t_;                    \
+    }                                                                             \
+  } while (0)
+#else
+#define MOE_STAMP(i) \
+  do {               \
+  } while (0)
+#endif
+
 template <int KMAX, class F>
 __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -289,6 +308,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   uint32_t* sm_words = reinterpret_cast<uint32_t*>(smem + L.words);
   const int ctid = threadIdx.x;                    // consumer thread index
   const int ncons = kFusedConsumers * 32;
+  if (threadIdx.x == 0) MOE_STAMP(MOE_TL_ENTRY);
   if (warp == kFusedConsumers && lane == 0) {
     // the tensor maps are kernel parameters: fetch them while upstream work drains
     asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tm_codes) : "memory");
@@ -306,6 +326,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   }
   __syncthreads();
   pdl_wait();      // x, topk_ids and topk_w come from upstream work
+  if (threadIdx.x == 0) MOE_STAMP(MOE_TL_INPUTS);
   // the routing first: every warp builds the expert schedule itself
   WarpSchedule<KMAX> s;
   s.load(p.ids, 1, p.k);
@@ -331,6 +352,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   DownWalk dw;
   dw.rows(p);
   s.finish(p.E, sm_words + warp * 32, p.err);
+  if (warp == kFusedConsumers && lane == 0) MOE_STAMP(MOE_TL_ROUTED);
   const int nU = s.n_unique;
   const GuStageLayout lay(KB, KC);
 
@@ -354,6 +376,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
       if (gw.valid) {
         const int e = s.expert(gw.u);   // warp-collective
         if (lane == 0) {
+          if (gi == 0) MOE_STAMP(MOE_TL_FIRST_ISSUE);
           // four tensor copies: the stage's gate rows, up rows, and their
           // scales (full boxes; rows past the expert are never read)
           mbar_expect_tx(bar, 2u * kFusedNeurons * KB + 2u * kFusedNeurons * (KC >> 5));
@@ -382,6 +405,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
         dw.next();
       }
     }
+    if (lane == 0) MOE_STAMP(MOE_TL_ISSUE_DONE);
     // the next launch may start its setup (off this warp's critical path)
     pdl_trigger();
     // never leave with copies in flight
@@ -442,6 +466,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     #pragma unroll 1
     for (; gw.valid; gw.next(), rg.next()) {
       if (!dead) dead = !mbar_wait(&full_g[rg.slot], rg.phase, p.err);
+      if (threadIdx.x == 0 && gw.st == 0 && gw.kc == 0) MOE_STAMP(MOE_TL_FIRST_LANDED);
       if (warp < gw.nn && !dead) {
         const uint8_t* base = ring_g + (size_t)rg.slot * p.slot_g;
         #pragma unroll 1
@@ -513,14 +538,20 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   bool have = dw.valid;
   // every h value of every CTA is written before any CTA reads h; the first
   // chunk is prepared while the other CTAs arrive
+  if (ctid == 0) MOE_STAMP(MOE_TL_GATE_UP_DONE);
   named_sync(1, ncons);
-  if (ctid == 0) grid_arrive(p.bar_ctr);
+  if (ctid == 0) {
+    MOE_STAMP(MOE_TL_ARRIVING);
+    grid_arrive(p.bar_ctr);
+  }
   if (have) {
     chunk_tables();
     chunk_wait();
   }
   if (ctid == 0) {
+    MOE_STAMP(MOE_TL_DOWN_LANDED);
     if (!grid_wait(p.bar_ctr, *bar_target, p.err)) dead = true;
+    MOE_STAMP(MOE_TL_BARRIER);
     // every unique expert's h row, one bulk copy each (the async proxy reads
     // what other CTAs' generic stores wrote: fence between the proxies)
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -538,6 +569,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     tf[t] = cf[u] * stage_block_f16(v, hs + 64 * t, b);
   }
   named_sync(1, ncons);   // h staged
+  if (ctid == 0) MOE_STAMP(MOE_TL_H_STAGED);
   {
     const int wI = warp * IB, wS = warp * nbI;
     #pragma unroll 1
@@ -576,6 +608,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
       for (int r = dw.r0 + ctid; r < dw.r1; r += ncons) p.y[r] = 0;
     }
   }
+  if (ctid == 0) MOE_STAMP(MOE_TL_DOWN_DONE);
 }
 
 }  // namespace moe

@@ -91,3 +91,20 @@ def test_null_handle_and_null_config(lib):
     assert lib.moe_decode_get_error_stream(None, None, None) == 1
     assert lib.moe_decode_destroy(None) == 0
     assert lib.moe_decode_kernel_name(None, 1, 0) == b""
+
+
+def test_timeline_library_exports_its_header():
+    # the MOE_TIMELINE build exports every call of both headers
+    import __graft_entry__
+    b = __graft_entry__._build_module()
+    if b.stale(b.OUT_TIMELINE):
+        b.build(timeline=True)
+    tl = ctypes.CDLL(b.OUT_TIMELINE)
+    text = open(os.path.join(ROOT, "include", "moe_decode_timeline.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+    assert "moe_decode_layer_timeline" in names
+    for n in names + declared_functions():
+        assert hasattr(tl, n), n
+    tl.moe_decode_timeline_ctas.argtypes = [ctypes.c_void_p]
+    assert tl.moe_decode_timeline_ctas(None) == -1
