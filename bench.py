@@ -26,10 +26,16 @@ oracle on one host thread and on every core of the process's affinity set
 3: Zipf-skewed T=32, 4: large experts T=16), for reports; the default line is
 workload 1. --format mxfp4 stores the same weights as MXFP4 (E2M1 codes two
 to a byte, the same UE8M0 scales): half the code bytes per step.
+--tokens T runs the workload's layer at T tokens per step, and --path warp or
+tensor forces output-centric warp decode or the expert-centric tensor-core
+path (auto: the tensor-core path from 64 tokens) -- the crossover study. On
+the tensor-core path the roofline line covers the whole step (its four
+launches against the step's weight bytes).
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import multiprocessing
@@ -72,6 +78,10 @@ def parse():
     # the other configurations, for reports (the default line is workload 1)
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--format", default="mxfp8", choices=sorted(wl.FORMATS))
+    # the crossover study: the workload's layer at another batch size, and
+    # which form the layer takes (auto: the tensor-core path from 64 tokens)
+    ap.add_argument("--tokens", type=int, default=0, help="tokens per step (default: the workload's T)")
+    ap.add_argument("--path", default="auto", choices=["auto", "warp", "tensor"])
     return ap.parse_args()
 
 
@@ -265,7 +275,7 @@ def cpu_baseline(w, seed, experts, budget_s, fmt):
 
 
 def run_reference(args, rank, world):
-    w = wl.workload(args.workload)
+    w = bench_workload(args)
     seed = wl.seed_of(args.workload)
     if rank != 0:
         return
@@ -303,8 +313,19 @@ def run_reference(args, rank, world):
 # our arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args, rank, world, local):
+def bench_workload(args):
+    """The workload, at --tokens tokens per step when given (same layer and
+    seeds, a name that says the batch size)."""
     w = wl.workload(args.workload)
+    if args.tokens and args.tokens != w.T:
+        w = dataclasses.replace(w, T=args.tokens,
+                                name=f"decode E{w.E} k{w.k} H{w.H} I{w.I} T{args.tokens}"
+                                     + (f" zipf{w.zipf}" if w.zipf else ""))
+    return w
+
+
+def run_ours(args, rank, world, local):
+    w = bench_workload(args)
     seed = wl.seed_of(args.workload)
     K, W, L = args.steps, args.warmup, args.layers
     T, E, k, H, I = w.T, w.E, w.k, w.H, w.I
@@ -349,7 +370,9 @@ def run_ours(args, rank, world, local):
     for _ in range(L):
         t = [b.clone() for b in base]
         layers.append((t, MoEDecode(*t, k=k, max_T=T, fmt=fmt)))
+        layers[-1][1].set_path(args.path)
     del base
+    path = layers[0][1].path(T)
 
     # per-step activations and routing (routing by the library's router)
     nsteps = W + K
@@ -395,11 +418,13 @@ def run_ours(args, rank, world, local):
         return g
 
     # at T = 1 the layer is one persistent launch per step (both projections);
-    # otherwise two launches, of which the gate/up kernel is the larger
-    fused = T == 1 and layers[0][1].fused_single_token
+    # on the tensor-core path four launches per group of 256 tokens, timed as
+    # a whole; otherwise two launches, of which the gate/up kernel is the larger
+    fused = path == "warp" and T == 1 and layers[0][1].fused_single_token
+    tensor = path == "tensor"
     g_warm = capture(range(W))
     g_main = capture(range(W, W + K))
-    g_gu = None if fused else capture(range(W, W + K), only_gate_up=True)
+    g_gu = None if fused or tensor else capture(range(W, W + K), only_gate_up=True)
     stream = torch.cuda.current_stream()
 
     # a cold single layer: one step of the first layer copy, replayed after an
@@ -445,12 +470,12 @@ def run_ours(args, rank, world, local):
         # R replays of the K-step graph, each bracketed by a barrier and a
         # synchronize; the line reports the median replay
         dts = [timed(g_main) for _ in range(R)]
-        dt_gus = None if fused else [timed(g_gu) for _ in range(max(3, R // 3))]
+        dt_gus = None if g_gu is None else [timed(g_gu) for _ in range(max(3, R // 3))]
         timed_cold(10)
         colds = timed_cold(max(1, args.cold))
     clocks = clk.summary()
     dt = statistics.median(dts)
-    dt_gu = None if fused else statistics.median(dt_gus)
+    dt_gu = None if g_gu is None else statistics.median(dt_gus)
     dt_max = reduce_max(dt, world)
     per_step = np.array(dts) / K * 1e6
     spread = {"replays": R, "median_us": float(np.median(per_step)),
@@ -474,6 +499,13 @@ def run_ours(args, rank, world, local):
         launch_s = dt / K
         achieved = float(bytes_step[W:].mean()) / launch_s / 1e9
         launches = K
+    elif tensor:
+        # the whole step: the unique experts' weight bytes over all four
+        # launches (moe_tc_prep, moe_tc_gate_up, moe_tc_down, moe_tc_combine)
+        kernel = "moe_tc_prep+moe_tc_gate_up+moe_tc_down+moe_tc_combine"
+        launch_s = dt / K
+        achieved = float(bytes_step[W:].mean()) / launch_s / 1e9
+        launches = 4 * K * (-(-T // 256))
     else:
         kernel = layers[0][1].kernel_name(T, "gate_up")
         launch_s = dt_gu / K
@@ -490,6 +522,8 @@ def run_ours(args, rank, world, local):
     wh = w_all.cpu().pin_memory()
     yh = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     e2e_layers = [MoEDecode(*t, k=k, max_T=T, fmt=fmt) for t, _ in layers]
+    for lay in e2e_layers:
+        lay.set_path(args.path)
     for s in range(min(W, 10)):
         e2e_layers[s % L].forward_host(xh[s], ih[s], wh[s], yh)
     barrier(world)
@@ -511,12 +545,14 @@ def run_ours(args, rank, world, local):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": 1e3 * dt_max / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if tensor else "f32", "data": "synthetic",
             "config": {
                 "workload": w.name, "E": E, "k": k, "H": H, "I": I, "T": T,
                 "weights": ("MXFP4 (E2M1 two per byte + UE8M0 per 32)" if fmt == "mxfp4" else
                             "MXFP8 (E4M3 + UE8M0 per 32)")
-                           + ", bf16 activations, FP32 accumulate"
+                           + (", decoded exactly to bf16, bf16 activations, tcgen05.mma with"
+                              " FP32 accumulators" if tensor else
+                              ", bf16 activations, FP32 accumulate")
                            + (" (random bytes generated on the device: timing only)" if big else ""),
                 "layers_rotated": L,
                 "l2": f"inputs larger than L2: {L} resident layer copies "
@@ -525,6 +561,8 @@ def run_ours(args, rank, world, local):
                 "timing": f"median of {R} replays of a K-step CUDA graph, each bracketed by "
                           "CUDA events on the replay stream (barrier + synchronize around each)",
                 "parallelism": f"replicas x{world}",
+                "path": "tensor cores (expert-centric, tcgen05)" if tensor else
+                        "warp decode (output-centric)",
             },
             "hbm_gbs": hbm_gbs,
             "step_us": spread,

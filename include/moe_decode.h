@@ -185,6 +185,21 @@ moe_status_t moe_down(moe_decode_t handle, int32_t T, const uint16_t* h,
  * grid barrier (a bounded wait; on timeout it sets MOE_DEVICE_TIMEOUT) once h
  * is written. h is still written to the caller's buffer. Such calls on one
  * handle must not run concurrently (they share the handle's counters).
+ * With T >= 64 tokens (or any T after moe_decode_set_path(handle,
+ * MOE_PATH_TENSOR)), when moe_decode_tensor_path(handle) is 1, the layer runs
+ * expert-centric on the tensor cores instead, in groups of up to 256 tokens
+ * (the warp-decode post, "Warp decode and Composer training": large batches
+ * favour packing tokens per expert; the operand-swapped MMA is the GC-MoE
+ * summary's, onedev.kr/papers/1690, "How it is used"). Per group, four
+ * launches: moe_tc_prep (the unique experts, each one's (token, slot) pairs,
+ * x gathered into expert order), moe_tc_gate_up and moe_tc_down (weights
+ * decoded exactly to bf16 into tensor memory as the A operand of
+ * tcgen05.mma kind::f16, 128 weight rows by up to 64 pairs a tile, FP32
+ * accumulators in tensor memory), moe_tc_combine (the routing-weighted sum
+ * in slot order). Every unique expert is streamed once per group. h is
+ * written to the caller's buffer as on the other path. The path keeps a
+ * workspace sized at create and is not thread-safe across concurrent calls
+ * on one handle (they share it); calls on one stream are ordered.
  */
 moe_status_t moe_decode_layer(moe_decode_t handle, int32_t T, const uint16_t* x,
                               const int32_t* topk_ids, const float* topk_w,
@@ -241,13 +256,46 @@ int32_t moe_decode_version(void);
 int32_t moe_decode_fused_layer(moe_decode_t handle);
 
 /*
+ * Which form moe_decode_layer and moe_decode_forward_host take:
+ *   MOE_PATH_AUTO    (the default) the tensor-core path from 64 tokens when
+ *                    the handle supports it, output-centric warp decode below
+ *   MOE_PATH_WARP    always warp decode (the one-launch kernel at T = 1)
+ *   MOE_PATH_TENSOR  always the tensor-core path; MOE_ERR_UNSUPPORTED_SHAPE
+ *                    when moe_decode_tensor_path(handle) is 0
+ * moe_gate_up and moe_down always run warp decode. Not synchronised with
+ * calls in flight on other threads.
+ */
+#define MOE_PATH_AUTO 0
+#define MOE_PATH_WARP 1
+#define MOE_PATH_TENSOR 2
+moe_status_t moe_decode_set_path(moe_decode_t handle, int32_t path);
+
+/* The path (MOE_PATH_WARP or MOE_PATH_TENSOR) a layer call with T tokens
+ * takes on this handle; -1 for a NULL handle or T < 1. */
+int32_t moe_decode_path(moe_decode_t handle, int32_t T);
+
+/*
+ * Diagnostic: 1 when the handle can run the tensor-core path, 0 when not, -1
+ * for a NULL handle. It needs max_T >= 1, H a multiple of 512, I a multiple
+ * of 128, 16-byte aligned scale arrays, and weights that all decode to normal
+ * bf16 values, so that the decode is exact: every scale code in 10..142
+ * (MXFP8) or 2..142 (MXFP4), and no E4M3 NaN code (checked once, at create,
+ * by a pass over both projections; the weights must not change afterwards).
+ * Its workspace, allocated at create, holds min(max_T, 256) * k pairs: x and
+ * h in expert order (bf16) and FP32 partial rows of y, (2H + 2I + 4H) bytes
+ * a pair, plus the schedule.
+ */
+int32_t moe_decode_tensor_path(moe_decode_t handle);
+
+/*
  * Diagnostic: the name of the kernel that moe_gate_up (which = 0) or moe_down
  * (which = 1) launches for T tokens on this handle (for T > 32, for each
  * group of 32): "moe_gate_up_tma", "moe_gate_up_3d_batched_xs" or
  * "moe_gate_up_3d_batched"; "moe_down_mma", "moe_down_tma" or
- * "moe_down_3d_batched". A static string; "" for a NULL handle, T <= 0 or
- * another `which`. (moe_decode_layer with T = 1 uses moe_layer_fused_t1 when
- * moe_decode_fused_layer says so.)
+ * "moe_down_3d_batched"; "moe_tc_gate_up" and "moe_tc_down" when a layer
+ * call with T tokens takes the tensor-core path. A static string; "" for a
+ * NULL handle, T <= 0 or another `which`. (moe_decode_layer with T = 1 uses
+ * moe_layer_fused_t1 when moe_decode_fused_layer says so.)
  */
 const char* moe_decode_kernel_name(moe_decode_t handle, int32_t T, int32_t which);
 

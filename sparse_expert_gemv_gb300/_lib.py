@@ -18,6 +18,9 @@ MOE_DEVICE_TIMEOUT = 0x2
 MOE_FLAG_NO_PDL = 0x1
 MOE_FLAG_HOST_COPY = 0x2
 MOE_FLAG_MXFP4 = 0x4
+MOE_PATH_AUTO = 0
+MOE_PATH_WARP = 1
+MOE_PATH_TENSOR = 2
 MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 STATUS_NAMES = {
@@ -69,6 +72,9 @@ SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [_st]),
     "moe_decode_version": (_i32, []),
     "moe_decode_fused_layer": (_i32, [_p]),
+    "moe_decode_set_path": (_st, [_p, _i32]),
+    "moe_decode_path": (_i32, [_p, _i32]),
+    "moe_decode_tensor_path": (_i32, [_p]),
     "moe_decode_kernel_name": (ctypes.c_char_p, [_p, _i32, _i32]),
     "moe_decode_plan": (_st, [ctypes.POINTER(MoEConfig), _i32, _i32, _i32, ctypes.POINTER(MoEPlan)]),
     "moe_decode_arm_barrier_timeout": (_st, [_p]),

@@ -19,6 +19,7 @@
 #include "moe_gate_up_mma.cuh"
 #include "moe_kernels.cuh"
 #include "moe_layer_fused.cuh"
+#include "moe_tc.cuh"
 
 namespace {
 
@@ -62,6 +63,22 @@ struct moe_decode {
   cudaEvent_t done_ev;
   bool done_recorded;
   cudaStream_t aux;
+  // the expert-centric tensor-core path (moe_tc.cuh): whether it can run
+  // (shape, alignment, and every weight decoding to a normal bf16), which
+  // path calls take (MOE_PATH_*), its workspace for min(max_T, 256) * k
+  // pairs, its tensor maps (W_gateup codes and scales, W_down codes, xg, hg),
+  // ring depths and shared-memory sizes
+  bool tc_ok;
+  int path;
+  void* tc_mem;
+  moe::TcWork tcw;
+  CUtensorMap tm_tc_gu;
+  CUtensorMap tm_tc_gus;
+  CUtensorMap tm_tc_dn;
+  CUtensorMap tm_tc_x;
+  CUtensorMap tm_tc_h;
+  int tc_R_gu, tc_R_dn;
+  size_t tc_smem_gu, tc_smem_dn;
   // staging buffers of moe_decode_forward_host (max_T tokens)
   uint16_t* d_x;
   int32_t* d_ids;
@@ -698,6 +715,229 @@ moe_status_t fused_layer(moe_decode* m, const uint16_t* x, const int32_t* ids, c
   return launch_fused(m, fp, smem, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// ---- expert-centric tensor-core path (moe_tc.cuh) --------------------------
+
+// Tokens from which MOE_PATH_AUTO takes the tensor-core path.
+constexpr int kTcAutoMinTokens = 64;
+
+// Shapes the path's kernels cover: whole 128-row tiles of I and H, gate/up
+// scale chunks of 512 elements, 16-byte aligned scale arrays, and TMA row
+// coordinates (E * 2I, E * H) that fit an int.
+bool tc_shape_ok(const moe_decode* m) {
+  const moe_decode_config_t& c = m->cfg;
+  return c.H % 512 == 0 && c.I % 128 == 0 && aligned(m->sgu, 16) && aligned(m->sd, 16) &&
+         (int64_t)c.E * 2 * c.I < (int64_t)INT32_MAX && (int64_t)c.E * c.H < (int64_t)INT32_MAX;
+}
+
+int tc_pairs(const moe_decode* m) { return std::min(m->cfg.max_T, moe::kTcMaxTokens) * m->cfg.k; }
+
+// Whether every weight decodes to a normal bf16 (scale codes in range, no
+// E4M3 NaN code): one pass over both projections' codes and scales. False
+// with ok = false when a CUDA call failed.
+bool tc_weights_exact(const moe_decode* m, bool& ok) {
+  const moe_decode_config_t& c = m->cfg;
+  const int CB = code_bytes_per_block(m);
+  uint32_t* d = nullptr;
+  const uint32_t init[4] = {0xFFFFFFFFu, 0u, 0u, 0u};
+  uint32_t h[4] = {};
+  const size_t gu_scales = (size_t)c.E * 2 * c.I * (c.H / 32);
+  const size_t dn_scales = (size_t)c.E * c.H * (c.I / 32);
+  const size_t gu_codes = gu_scales * CB, dn_codes = dn_scales * CB;
+  const dim3 grid(m->num_sms * 4), block(256);
+  (void)cudaGetLastError();   // a launch error below must be this pass's own
+  ok = cudaMalloc(&d, 16) == cudaSuccess &&
+       cudaMemcpy(d, init, 16, cudaMemcpyHostToDevice) == cudaSuccess;
+  if (ok) {
+    moe::moe_tc_scan<<<grid, block>>>(reinterpret_cast<const uint4*>(m->wgu), gu_codes / 16,
+                                      reinterpret_cast<const uint4*>(m->sgu), gu_scales / 16,
+                                      is_fp4(m) ? 0 : 1, d);
+    moe::moe_tc_scan<<<grid, block>>>(reinterpret_cast<const uint4*>(m->wd), dn_codes / 16,
+                                      reinterpret_cast<const uint4*>(m->sd), dn_scales / 16,
+                                      is_fp4(m) ? 0 : 1, d);
+    ok = cudaGetLastError() == cudaSuccess &&
+         cudaMemcpy(h, d, 16, cudaMemcpyDeviceToHost) == cudaSuccess;
+  }
+  if (d) cudaFree(d);
+  const uint32_t lo = is_fp4(m) ? moe::kTcScaleMinFp4 : moe::kTcScaleMinFp8;
+  return ok && h[0] >= lo && h[1] <= (uint32_t)moe::kTcScaleMax && h[2] == 0u;
+}
+
+// A [rows, cols] tensor of `dtype` (elem bytes each, rows `pitch` bytes
+// apart) read in boxes of box_rows x box_cols.
+bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, uint64_t cols,
+               uint64_t rows, uint64_t pitch, uint32_t box_cols, uint32_t box_rows,
+               CUtensorMapSwizzle swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(tm, dtype, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Deepest weight-code ring (at most 32 slots) whose kernel fits the
+// shared-memory limit, with the 1024-byte alignment slack; 0 when none does.
+int tc_ring(const moe_decode* m, bool down, size_t& smem) {
+  const int RB = is_fp4(m) ? moe::TcFp4::kStageRowBytes : moe::TcFp8::kStageRowBytes;
+  for (int R = 32; R >= 4; --R) {
+    const moe::TcSmem L(down, RB, R, m->cfg.I);
+    if ((size_t)L.total + 1024 <= m->smem_per_block) {
+      smem = (size_t)L.total + 1024;
+      return R;
+    }
+  }
+  return 0;
+}
+
+template <class F>
+cudaError_t set_tc_attributes(size_t gu, size_t dn, size_t prep) {
+  cudaError_t e = cudaFuncSetAttribute(moe::moe_tc_gate_up<F>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gu);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(moe::moe_tc_down<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)dn);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(moe::moe_tc_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)prep);
+  return e;
+}
+
+// Sets m->tc_ok when the path can run for this handle: allocates its
+// workspace and encodes its tensor maps. False only when a CUDA call failed.
+bool tc_setup(moe_decode* m) {
+  m->tc_ok = false;
+  const moe_decode_config_t& c = m->cfg;
+  if (c.max_T < 1 || !tc_shape_ok(m)) return true;
+  bool ok = true;
+  if (!tc_weights_exact(m, ok)) return ok;
+  size_t smem_gu = 0, smem_dn = 0;
+  m->tc_R_gu = tc_ring(m, false, smem_gu);
+  m->tc_R_dn = tc_ring(m, true, smem_dn);
+  const int Pw = tc_pairs(m);
+  // moe_tc_prep's dynamic shared memory for a full group (its 16 static
+  // bytes come on top)
+  const size_t smem_prep = moe::tc_prep_smem(Pw, c.E);
+  if (m->tc_R_gu == 0 || m->tc_R_dn == 0 || smem_prep + 256 > m->smem_per_block) return true;
+  m->tc_smem_gu = smem_gu;
+  m->tc_smem_dn = smem_dn;
+  // workspace: schedule ints, then xg, hg and yp (256-byte aligned)
+  const int maxC = std::min(c.E, Pw) + Pw / moe::kTcCols + 1;
+  auto up256 = [](size_t v) { return (v + 255) / 256 * 256; };
+  const size_t ints = up256((size_t)(4 + 3 * maxC + 2 * Pw) * 4);
+  const size_t xg = up256((size_t)Pw * c.H * 2), hg = up256((size_t)Pw * c.I * 2);
+  const size_t yp = up256((size_t)Pw * c.H * 4);
+  if (cudaMalloc(&m->tc_mem, ints + xg + hg + yp) != cudaSuccess ||
+      cudaMemset(m->tc_mem, 0, ints + xg + hg + yp) != cudaSuccess)
+    return false;
+  uint8_t* b = static_cast<uint8_t*>(m->tc_mem);
+  int* iw = reinterpret_cast<int*>(b);
+  m->tcw.hdr = iw;
+  m->tcw.chunk_e = iw + 4;
+  m->tcw.chunk_p0 = m->tcw.chunk_e + maxC;
+  m->tcw.chunk_n = m->tcw.chunk_p0 + maxC;
+  m->tcw.pair_slot = m->tcw.chunk_n + maxC;
+  m->tcw.slot_pair = m->tcw.pair_slot + Pw;
+  m->tcw.xg = reinterpret_cast<uint16_t*>(b + ints);
+  m->tcw.hg = reinterpret_cast<uint16_t*>(b + ints + xg);
+  m->tcw.yp = reinterpret_cast<float*>(b + ints + xg + hg);
+  const int CB = code_bytes_per_block(m);
+  const int RB = is_fp4(m) ? moe::TcFp4::kStageRowBytes : moe::TcFp8::kStageRowBytes;
+  const CUtensorMapSwizzle sw = is_fp4(m) ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const uint64_t gu_rows = (uint64_t)c.E * 2 * c.I, dn_rows = (uint64_t)c.E * c.H;
+  const uint64_t gu_rb = (uint64_t)c.H / 32 * CB, dn_rb = (uint64_t)c.I / 32 * CB;
+  const bool maps =
+      encode_2d(&m->tm_tc_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, m->wgu, gu_rb, gu_rows, gu_rb, RB,
+                moe::kTcRows, sw) &&
+      encode_2d(&m->tm_tc_gus, CU_TENSOR_MAP_DATA_TYPE_UINT8, m->sgu, c.H / 32, gu_rows,
+                c.H / 32, 16, moe::kTcRows, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+      encode_2d(&m->tm_tc_dn, CU_TENSOR_MAP_DATA_TYPE_UINT8, m->wd, dn_rb, dn_rows, dn_rb, RB,
+                moe::kTcRows, sw) &&
+      encode_2d(&m->tm_tc_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, m->tcw.xg, c.H, Pw, (uint64_t)c.H * 2,
+                moe::kTcK, moe::kTcBBox, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      encode_2d(&m->tm_tc_h, CU_TENSOR_MAP_DATA_TYPE_UINT16, m->tcw.hg, c.I, Pw, (uint64_t)c.I * 2,
+                moe::kTcK, moe::kTcBBox, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!maps) return true;
+  const cudaError_t e =
+      is_fp4(m) ? set_tc_attributes<moe::TcFp4>(smem_gu, smem_dn, smem_prep)
+                : set_tc_attributes<moe::TcFp8>(smem_gu, smem_dn, smem_prep);
+  if (e != cudaSuccess) return false;
+  m->tc_ok = true;
+  return true;
+}
+
+// Whether a call with T tokens takes the tensor-core path.
+bool use_tc(const moe_decode* m, int T) {
+  if (!m->tc_ok || m->path == MOE_PATH_WARP) return false;
+  return m->path == MOE_PATH_TENSOR || T >= kTcAutoMinTokens;
+}
+
+template <class F>
+moe_status_t tc_layer_f(moe_decode* m, int T, const uint16_t* x, const int32_t* ids,
+                        const float* w, uint16_t* h, uint16_t* y, cudaStream_t s) {
+  const moe_decode_config_t& c = m->cfg;
+  const bool pdl = use_pdl(m);
+  for (int t0 = 0; t0 < T; t0 += moe::kTcMaxTokens) {
+    const int Tg = std::min(moe::kTcMaxTokens, T - t0);
+    const int P = Tg * c.k;
+    moe::TcPrepParams pp = {};
+    pp.x = x + (size_t)t0 * c.H;
+    pp.ids = ids + (size_t)t0 * c.k;
+    pp.h = h + (size_t)t0 * c.k * c.I;
+    pp.err = m->d_err;
+    pp.w = m->tcw;
+    pp.T = Tg;
+    pp.k = c.k;
+    pp.E = c.E;
+    pp.H = c.H;
+    pp.I = c.I;
+    moe::TcParams gp = {};
+    gp.tm_w = m->tm_tc_gu;
+    gp.tm_s = m->tm_tc_gus;
+    gp.tm_b = m->tm_tc_x;
+    gp.sd = m->sd;
+    gp.h = pp.h;
+    gp.err = m->d_err;
+    gp.w = m->tcw;
+    gp.E = c.E;
+    gp.H = c.H;
+    gp.I = c.I;
+    gp.R = m->tc_R_gu;
+    moe::TcParams dp = gp;
+    dp.tm_w = m->tm_tc_dn;
+    dp.tm_b = m->tm_tc_h;
+    dp.R = m->tc_R_dn;
+    moe::TcCombineParams cp = {};
+    cp.tw = w + (size_t)t0 * c.k;
+    cp.y = y + (size_t)t0 * c.H;
+    cp.w = m->tcw;
+    cp.T = Tg;
+    cp.k = c.k;
+    cp.H = c.H;
+    const int G = m->num_sms;
+    if (launch(moe::moe_tc_prep, dim3(std::min(G, P)), dim3(moe::kTcPrepThreads),
+               moe::tc_prep_smem(P, c.E), s, pdl, pp) != cudaSuccess ||
+        launch(moe::moe_tc_gate_up<F>, dim3(G), dim3(moe::kTcGuThreads), m->tc_smem_gu, s, pdl,
+               gp) != cudaSuccess ||
+        launch(moe::moe_tc_down<F>, dim3(G), dim3(moe::kTcDnThreads), m->tc_smem_dn, s, pdl,
+               dp) != cudaSuccess ||
+        launch(moe::moe_tc_combine, dim3((c.H + 4 * moe::kTcCombineThreads - 1) /
+                                             (4 * moe::kTcCombineThreads),
+                                         Tg),
+               dim3(moe::kTcCombineThreads), 0, s, pdl, cp) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status_t tc_layer(moe_decode* m, int T, const uint16_t* x, const int32_t* ids, const float* w,
+                      uint16_t* h, uint16_t* y, cudaStream_t s) {
+  return is_fp4(m) ? tc_layer_f<moe::TcFp4>(m, T, x, ids, w, h, y, s)
+                   : tc_layer_f<moe::TcFp8>(m, T, x, ids, w, h, y, s);
+}
+
 // ---- per-call token chunking -----------------------------------------------
 
 // Tokens per gate/up launch: groups of 32, or, when a group's x does not fit
@@ -766,6 +1006,7 @@ moe_status_t down_chunks(moe_decode* m, int T, const uint16_t* h, const int32_t*
 // The layer's launches for T >= 1 tokens (arguments checked by the caller).
 moe_status_t layer_enqueue(moe_decode* m, int T, const uint16_t* x, const int32_t* topk_ids,
                            const float* topk_w, uint16_t* h, uint16_t* y, cudaStream_t s) {
+  if (use_tc(m, T)) return tc_layer(m, T, x, topk_ids, topk_w, h, y, s);
   if (T == 1 && m->fused_ok) return fused_layer(m, x, topk_ids, topk_w, h, y, s);
   moe_status_t st;
   if (T <= moe::kMaxTokensPerLaunch) {
@@ -842,6 +1083,7 @@ void free_all(moe_decode* m) {
   cudaFree(m->d_w);
   cudaFree(m->d_h);
   cudaFree(m->d_y);
+  cudaFree(m->tc_mem);
   delete m;
 }
 
@@ -885,6 +1127,7 @@ moe_status_t moe_decode_create(const moe_decode_config_t* cfg, const uint8_t* w_
   ok = ok && query_fused(m);
   m->gu_tma_ok = ok && encode_gu_tma_maps(m);
   m->dn_tma_ok = ok && encode_dn_tma_maps(m);
+  ok = ok && tc_setup(m);
 
 
   ok = ok && set_down_attributes() == cudaSuccess;
@@ -1056,6 +1299,20 @@ int32_t moe_decode_version(void) { return kVersion; }
 
 int32_t moe_decode_fused_layer(moe_decode_t m) { return m ? (m->fused_ok ? 1 : 0) : -1; }
 
+moe_status_t moe_decode_set_path(moe_decode_t m, int32_t path) {
+  if (!m || path < MOE_PATH_AUTO || path > MOE_PATH_TENSOR) return MOE_ERR_INVALID_ARG;
+  if (path == MOE_PATH_TENSOR && !m->tc_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
+  m->path = path;
+  return MOE_OK;
+}
+
+int32_t moe_decode_path(moe_decode_t m, int32_t T) {
+  if (!m || T < 1) return -1;
+  return use_tc(m, T) ? MOE_PATH_TENSOR : MOE_PATH_WARP;
+}
+
+int32_t moe_decode_tensor_path(moe_decode_t m) { return m ? (m->tc_ok ? 1 : 0) : -1; }
+
 moe_status_t moe_decode_plan(const moe_decode_config_t* cfg, int32_t num_sms,
                              int32_t smem_per_block, int32_t T, moe_decode_plan_t* out) {
   if (!cfg || !out || num_sms < 1 || smem_per_block < 1 || T < 1) return MOE_ERR_INVALID_ARG;
@@ -1104,6 +1361,7 @@ moe_status_t moe_decode_plan(const moe_decode_config_t* cfg, int32_t num_sms,
 
 const char* moe_decode_kernel_name(moe_decode_t m, int32_t T, int32_t which) {
   if (!m || T <= 0 || (which != 0 && which != 1)) return "";
+  if (use_tc(m, T)) return which == 0 ? "moe_tc_gate_up" : "moe_tc_down";
   const int Tl = std::min<int>(T, moe::kMaxTokensPerLaunch);
   int SG = 0;
   size_t smem = 0;

@@ -9,7 +9,8 @@ import ctypes
 
 import torch
 
-from ._lib import MOE_FLAG_MXFP4, MoEConfig, check, lib
+from ._lib import (MOE_FLAG_MXFP4, MOE_PATH_AUTO, MOE_PATH_TENSOR, MOE_PATH_WARP, MoEConfig, check,
+                   lib)
 
 
 def _ptr(t: torch.Tensor | None) -> int:
@@ -101,6 +102,21 @@ class MoEDecode:
     def fused_single_token(self) -> bool:
         """True when one-token layer calls run as one persistent launch."""
         return lib.moe_decode_fused_layer(self._h) == 1
+
+    @property
+    def tensor_path(self) -> bool:
+        """True when this handle can run the expert-centric tensor-core path."""
+        return lib.moe_decode_tensor_path(self._h) == 1
+
+    def set_path(self, path: str) -> None:
+        """Which form layer calls take: "auto" (the tensor-core path from 64
+        tokens), "warp" or "tensor"."""
+        code = {"auto": MOE_PATH_AUTO, "warp": MOE_PATH_WARP, "tensor": MOE_PATH_TENSOR}[path]
+        check(lib.moe_decode_set_path(self._h, code), "moe_decode_set_path")
+
+    def path(self, T: int) -> str:
+        """The form a layer call with T tokens takes: "warp" or "tensor"."""
+        return {MOE_PATH_WARP: "warp", MOE_PATH_TENSOR: "tensor"}[lib.moe_decode_path(self._h, T)]
 
     def kernel_name(self, T: int, which: str) -> str:
         """The kernel moe_gate_up (which="gate_up") or moe_down ("down")

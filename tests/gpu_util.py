@@ -16,14 +16,21 @@ def tensor_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def device_weights(w: wl.Workload, experts: dict, device, fill_code=wl.NAN_CODE, fmt="mxfp8"):
+def device_weights(w: wl.Workload, experts: dict, device, fill_code=wl.NAN_CODE, fmt="mxfp8",
+                   fill="nan"):
     """Full [E, ...] device tensors; experts absent from `experts` hold NaN codes
     (MXFP8) or NaN scales (MXFP4, whose codes have no NaN), so a kernel that
-    reads them poisons exactly the outputs that used them."""
+    reads them poisons exactly the outputs that used them. With fill="finite"
+    they hold the value 1.0 * 2^-7 everywhere instead (code 0x38 or the E2M1
+    pair 0x22, scale 120): finite, so the tensor-core path stays available,
+    yet far from the seeded weights, so reading them still shows in the
+    outputs that used them."""
     E, H, I = w.E, w.H, w.I
     per = 2 if fmt == "mxfp4" else 1
     fill_scale = 127
-    if fmt == "mxfp4":
+    if fill == "finite":
+        fill_code, fill_scale = (0x22 if fmt == "mxfp4" else 0x38), 120
+    elif fmt == "mxfp4":
         fill_code, fill_scale = 0x77, 0xFF
     wgu = torch.full((E, 2 * I, H // per), fill_code, dtype=torch.uint8, device=device)
     sgu = torch.full((E, 2 * I, H // 32), fill_scale, dtype=torch.uint8, device=device)
