@@ -79,9 +79,9 @@ def parse():
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--format", default="mxfp8", choices=sorted(wl.FORMATS))
     # the crossover study: the workload's layer at another batch size, and
-    # which form the layer takes (auto: the tensor-core path from 64 tokens)
+    # which form the layer takes (auto: the library's choice)
     ap.add_argument("--tokens", type=int, default=0, help="tokens per step (default: the workload's T)")
-    ap.add_argument("--path", default="auto", choices=["auto", "warp", "tensor"])
+    ap.add_argument("--path", default="auto", choices=["auto", "warp", "warp-mma", "tensor"])
     return ap.parse_args()
 
 
@@ -366,11 +366,15 @@ def run_ours(args, rank, world, local):
     else:
         host = [np.stack([experts[e][i] for e in range(E)]) for i in range(4)]
         base = [torch.from_numpy(a).to(dev) for a in host]
+    # --path warp-mma: warp decode with the several-token warp-level MMA kernels
+    from sparse_expert_gemv_gb300 import MOE_FLAG_WARP_MMA
+    lib_path = "warp" if args.path == "warp-mma" else args.path
+    lib_flags = MOE_FLAG_WARP_MMA if args.path == "warp-mma" else 0
     layers = []
     for _ in range(L):
         t = [b.clone() for b in base]
-        layers.append((t, MoEDecode(*t, k=k, max_T=T, fmt=fmt)))
-        layers[-1][1].set_path(args.path)
+        layers.append((t, MoEDecode(*t, k=k, max_T=T, fmt=fmt, flags=lib_flags)))
+        layers[-1][1].set_path(lib_path)
     del base
     path = layers[0][1].path(T)
 
@@ -521,9 +525,9 @@ def run_ours(args, rank, world, local):
     ih = ids_all.cpu().pin_memory()
     wh = w_all.cpu().pin_memory()
     yh = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    e2e_layers = [MoEDecode(*t, k=k, max_T=T, fmt=fmt) for t, _ in layers]
+    e2e_layers = [MoEDecode(*t, k=k, max_T=T, fmt=fmt, flags=lib_flags) for t, _ in layers]
     for lay in e2e_layers:
-        lay.set_path(args.path)
+        lay.set_path(lib_path)
     for s in range(min(W, 10)):
         e2e_layers[s % L].forward_host(xh[s], ih[s], wh[s], yh)
     barrier(world)
@@ -562,7 +566,8 @@ def run_ours(args, rank, world, local):
                           "CUDA events on the replay stream (barrier + synchronize around each)",
                 "parallelism": f"replicas x{world}",
                 "path": "tensor cores (expert-centric, tcgen05)" if tensor else
-                        "warp decode (output-centric)",
+                        "warp decode (output-centric)"
+                        + (", several-token warp-level MMA kernels" if lib_flags else ""),
             },
             "hbm_gbs": hbm_gbs,
             "step_us": spread,

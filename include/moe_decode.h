@@ -71,6 +71,12 @@ typedef enum {
                                       the device staging buffers */
 #define MOE_FLAG_MXFP4 0x4u        /* the weights are MXFP4, not MXFP8 (see
                                       moe_decode_create) */
+#define MOE_FLAG_WARP_MMA 0x8u     /* warp-decode calls of 16 to 32 tokens form
+                                      their products on the warp-level MMA
+                                      (kernels moe_gate_up_tma, moe_down_mma):
+                                      faster when a few experts serve many of
+                                      the tokens, slower when each expert
+                                      serves one or two (the default then) */
 
 typedef struct {
   int32_t E;      /* experts, 1..1024 */
@@ -257,8 +263,10 @@ int32_t moe_decode_fused_layer(moe_decode_t handle);
 
 /*
  * Which form moe_decode_layer and moe_decode_forward_host take:
- *   MOE_PATH_AUTO    (the default) the tensor-core path from 64 tokens when
- *                    the handle supports it, output-centric warp decode below
+ *   MOE_PATH_AUTO    (the default) the tensor-core path when the handle
+ *                    supports it, T >= 16 and T * k >= 2 E (two or more
+ *                    routed slots per expert on average), output-centric
+ *                    warp decode otherwise
  *   MOE_PATH_WARP    always warp decode (the one-launch kernel at T = 1)
  *   MOE_PATH_TENSOR  always the tensor-core path; MOE_ERR_UNSUPPORTED_SHAPE
  *                    when moe_decode_tensor_path(handle) is 0

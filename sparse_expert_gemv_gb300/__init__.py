@@ -11,9 +11,10 @@ The compute lives in libmoe_decode.so (C ABI, include/moe_decode.h). This
 package is a thin ctypes binding: PyTorch supplies device memory and streams.
 """
 from ._lib import (LIB_PATH, MOE_DEVICE_BAD_ID, MOE_DEVICE_TIMEOUT, MOE_FLAG_HOST_COPY,
-                   MOE_FLAG_MXFP4, MOE_FLAG_NO_PDL, MoEConfig, MoEError, check, lib)
+                   MOE_FLAG_MXFP4, MOE_FLAG_NO_PDL, MOE_FLAG_WARP_MMA, MoEConfig, MoEError, check,
+                   lib)
 from .layer import MoEDecode
 
 __all__ = ["MoEDecode", "MoEError", "MoEConfig", "lib", "check", "LIB_PATH",
            "MOE_DEVICE_BAD_ID", "MOE_DEVICE_TIMEOUT", "MOE_FLAG_HOST_COPY", "MOE_FLAG_MXFP4",
-           "MOE_FLAG_NO_PDL"]
+           "MOE_FLAG_NO_PDL", "MOE_FLAG_WARP_MMA"]

@@ -18,6 +18,7 @@ MOE_DEVICE_TIMEOUT = 0x2
 MOE_FLAG_NO_PDL = 0x1
 MOE_FLAG_HOST_COPY = 0x2
 MOE_FLAG_MXFP4 = 0x4
+MOE_FLAG_WARP_MMA = 0x8
 MOE_PATH_AUTO = 0
 MOE_PATH_WARP = 1
 MOE_PATH_TENSOR = 2

@@ -124,7 +124,11 @@ bool use_pdl(const moe_decode* m) { return (m->cfg.flags & MOE_FLAG_NO_PDL) == 0
 bool is_fp4(const moe_decode* m) { return (m->cfg.flags & MOE_FLAG_MXFP4) != 0; }
 int code_bytes_per_block(const moe_decode* m) { return is_fp4(m) ? 16 : 32; }
 
-constexpr uint32_t kKnownFlags = MOE_FLAG_NO_PDL | MOE_FLAG_HOST_COPY | MOE_FLAG_MXFP4;
+constexpr uint32_t kKnownFlags =
+    MOE_FLAG_NO_PDL | MOE_FLAG_HOST_COPY | MOE_FLAG_MXFP4 | MOE_FLAG_WARP_MMA;
+
+// Whether several-token warp-decode calls may take the warp-level MMA kernels.
+bool warp_mma(const moe_decode* m) { return (m->cfg.flags & MOE_FLAG_WARP_MMA) != 0; }
 
 // ---- gate/up ---------------------------------------------------------------
 
@@ -181,11 +185,13 @@ cudaError_t launch_gate_up_tma(const moe_decode* m, const moe::GateUpParams& p, 
 // slots and shared memory where it has a ring.
 enum class GuKind { kTma, kXs, kL1 };
 GuKind gate_up_kind(const moe_decode* m, int T, int& SG, size_t& smem) {
-  // sixteen or more tokens whose x fits in shared memory beside a weight
-  // ring: tiles streamed by TMA, products on the warp-level MMA (one CTA per
-  // SM). With fewer tokens an expert rarely serves more than one or two, and
-  // the FP32 kernel below issues fewer instructions per weight byte.
-  if (T >= kGuTmaMinTokens && m->gu_tma_ok) {
+  // with MOE_FLAG_WARP_MMA, sixteen or more tokens whose x fits in shared
+  // memory beside a weight ring: tiles streamed by TMA, products on the
+  // warp-level MMA (one CTA per SM). It pays when an expert serves many
+  // tokens; where each serves one or two (uniform routing) the FP32 kernel
+  // below issues fewer instructions per weight byte (T = 16: 132 against
+  // 240 us a layer).
+  if (warp_mma(m) && T >= kGuTmaMinTokens && m->gu_tma_ok) {
     SG = gu_tma_slots(m, T, smem);
     if (SG >= 2) return GuKind::kTma;
   }
@@ -308,7 +314,8 @@ DnKind down_kind(const moe_decode* m, int T, int& SG, size_t& smem) {
   // fewer tokens an expert rarely serves more than one or two, and the
   // token-by-token kernel keeps more of the stream in flight; a warp per ring
   // slot: with few slots too few warps would reduce)
-  if (T >= kGuTmaMinTokens && m->dn_tma_ok && m->cfg.I / 32 * code_bytes_per_block(m) <= 1024) {
+  if (warp_mma(m) && T >= kGuTmaMinTokens && m->dn_tma_ok &&
+      m->cfg.I / 32 * code_bytes_per_block(m) <= 1024) {
     SG = dn_mma_slots(m, T, smem);
     if (SG >= kDnMmaMinSlots) return DnKind::kMma;
   }
@@ -717,8 +724,15 @@ moe_status_t fused_layer(moe_decode* m, const uint16_t* x, const int32_t* ids, c
 
 // ---- expert-centric tensor-core path (moe_tc.cuh) --------------------------
 
-// Tokens from which MOE_PATH_AUTO takes the tensor-core path.
-constexpr int kTcAutoMinTokens = 64;
+// MOE_PATH_AUTO takes the tensor-core path from kTcAutoMinTokens tokens when
+// they route at least kTcAutoSlotsPerExpert slots per expert on average.
+// Measured on one GB300 (E = 128, k = 8, H = 2048, I = 768, MXFP8, us a
+// layer, FP32 warp kernels / tensor-core path): uniform routing T = 16
+// 132 / 196, T = 24 200 / 228, T = 32 246 / 249, T = 64 689 / 271; Zipf-skewed
+// routing T = 16 129 / 100, T = 32 231 / 111. E = 256 at T = 16 (one slot per
+// two experts): 916 / 1887.
+constexpr int kTcAutoMinTokens = 16;
+constexpr int kTcAutoSlotsPerExpert = 2;
 
 // Shapes the path's kernels cover: whole 128-row tiles of I and H, gate/up
 // scale chunks of 512 elements, 16-byte aligned scale arrays, and TMA row
@@ -871,7 +885,8 @@ bool tc_setup(moe_decode* m) {
 // Whether a call with T tokens takes the tensor-core path.
 bool use_tc(const moe_decode* m, int T) {
   if (!m->tc_ok || m->path == MOE_PATH_WARP) return false;
-  return m->path == MOE_PATH_TENSOR || T >= kTcAutoMinTokens;
+  return m->path == MOE_PATH_TENSOR ||
+         (T >= kTcAutoMinTokens && T * m->cfg.k >= kTcAutoSlotsPerExpert * m->cfg.E);
 }
 
 template <class F>

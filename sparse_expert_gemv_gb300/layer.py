@@ -109,8 +109,9 @@ class MoEDecode:
         return lib.moe_decode_tensor_path(self._h) == 1
 
     def set_path(self, path: str) -> None:
-        """Which form layer calls take: "auto" (the tensor-core path from 64
-        tokens), "warp" or "tensor"."""
+        """Which form layer calls take: "auto" (the tensor-core path from 16
+        tokens when they route two or more slots per expert on average),
+        "warp" or "tensor"."""
         code = {"auto": MOE_PATH_AUTO, "warp": MOE_PATH_WARP, "tensor": MOE_PATH_TENSOR}[path]
         check(lib.moe_decode_set_path(self._h, code), "moe_decode_set_path")
 

@@ -102,3 +102,30 @@ class Case:
         w = self.w
         return oracle.layer(self.x64(), self.ids, self.tw, self.experts, w.E, w.H, w.I,
                             tokens=self.tokens, fmt=self.fmt)
+
+
+def check_layer_call(layer, case, x, ids, tw, y_two, fmt="mxfp8") -> None:
+    """The layer entry point on a case whose gate/up + down results (y_two)
+    were already checked: at T = 1 through the one-launch kernel, y against
+    the oracle; on the tensor-core path, h against the oracle's h and y
+    against the oracle's down projection of that h (the layer's y is defined
+    from its stored bf16 h, and the tensor cores' FP32 sums put a few more h
+    values on the other side of a bf16 rounding boundary than FMA chains
+    do); otherwise bit for bit the two-kernel result."""
+    w, S = case.w, case.tokens
+    h2 = torch.full((case.T, w.k, w.I), float("nan"), dtype=torch.bfloat16, device=x.device)
+    y2 = layer.layer(x, ids, tw, h=h2)
+    torch.cuda.synchronize()
+    ref = case.ref()
+    if case.T == 1 and layer.fused_single_token:
+        # one launch for both projections: its own sums, checked on their own
+        assert_within(tensor_to_f64(y2)[S], ref["y_spec"][S], tol_y(ref["y_spec"][S]),
+                      "y (one launch)")
+    elif layer.path(case.T) == "tensor":
+        hg = tensor_to_f64(h2)
+        assert_within(hg[S], ref["h_spec"][S], tol_h(ref["h_spec"][S]), "h (tensor cores)")
+        y_own = oracle.down(hg, case.ids, case.tw, case.experts, w.E, w.H, tokens=S, fmt=fmt)
+        assert_within(tensor_to_f64(y2)[S], y_own[S], tol_y(y_own[S]), "y (tensor cores)")
+    else:
+        assert torch.equal(y_two.view(torch.int16)[S], y2.view(torch.int16)[S]), \
+            "layer() differs from gate_up+down"

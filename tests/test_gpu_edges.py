@@ -367,7 +367,9 @@ def test_single_token_layer_barrier_timeout_is_reported(dev):
     (3, 3, 2048, 96, 17),     # every expert serves every token: three passes
 ])
 def test_several_token_tma_gate_up(dev, fmt, E, k, H, I, T):
-    s = Small(dev, E, k, H, I, T, seed=E * T, fmt=fmt)
+    from sparse_expert_gemv_gb300 import MOE_FLAG_WARP_MMA
+    s = Small(dev, E, k, H, I, T, seed=E * T, fmt=fmt, flags=MOE_FLAG_WARP_MMA)
+    s.layer.set_path("warp")        # layer calls too (the names are the layer call's kernels)
     assert s.layer.kernel_name(T, "gate_up") == "moe_gate_up_tma"
     s.check()
     ids = s.ids.copy()
@@ -399,11 +401,14 @@ def test_several_token_tma_gate_up(dev, fmt, E, k, H, I, T):
     (20, 4, 96, 2048, 3),     # I at its maximum, six row tiles
     (6, 3, 256, 128, 40),     # T > 32: two token groups
 ])
-def test_several_token_tma_down(dev, fmt, E, k, H, I, T):
-    s = Small(dev, E, k, H, I, T, seed=3 * E + T, fmt=fmt)
-    # fewer than 16 tokens: token by token; 16 or more (here a group of 32):
-    # each unique expert's rows once, on the MMA
-    assert s.layer.kernel_name(T, "down") == ("moe_down_mma" if T >= 16 else "moe_down_tma")
+@pytest.mark.parametrize("mma", [False, True])
+def test_several_token_tma_down(dev, fmt, E, k, H, I, T, mma):
+    from sparse_expert_gemv_gb300 import MOE_FLAG_WARP_MMA
+    s = Small(dev, E, k, H, I, T, seed=3 * E + T, fmt=fmt, flags=MOE_FLAG_WARP_MMA if mma else 0)
+    s.layer.set_path("warp")        # layer calls too (the names are the layer call's kernels)
+    # token by token; with MOE_FLAG_WARP_MMA and 16 or more tokens (here a
+    # group of 32) each unique expert's rows once, on the MMA
+    assert s.layer.kernel_name(T, "down") == ("moe_down_mma" if mma and T >= 16 else "moe_down_tma")
     s.check()
     ids = s.ids.copy()
     ids[0, 1] = ids[0, 0]           # duplicate: one distinct expert, weights summed
@@ -423,11 +428,15 @@ def test_several_token_tma_down(dev, fmt, E, k, H, I, T):
 def test_kernel_choice_by_workload(dev):
     # which kernels the seeded workloads' calls take (weights need not be real)
     from sparse_expert_gemv_gb300 import MoEDecode
+    # (NaN weights: the tensor-core path is unavailable, so the warp path's
+    # kernels are reported; the layer of workload 3 takes the tensor-core
+    # path when the weights allow it, see test_gpu_tc.py)
+    from sparse_expert_gemv_gb300 import MOE_FLAG_WARP_MMA
     want = {
         0: ("moe_gate_up_3d_batched", "moe_down_3d_batched"),       # T = 1, shapes below the ring kernels
         1: ("moe_gate_up_3d_batched", "moe_down_3d_batched"),       # T = 1 (moe_decode_layer: one launch)
         2: ("moe_gate_up_3d_batched_xs", "moe_down_tma"),
-        3: ("moe_gate_up_tma", "moe_down_mma"),
+        3: ("moe_gate_up_3d_batched_xs", "moe_down_tma"),
     }
     for c, (gu, dn) in want.items():
         w = wl.workload(c)
@@ -435,6 +444,13 @@ def test_kernel_choice_by_workload(dev):
             lay = MoEDecode(*device_weights(w, {}, dev, fmt=fmt), k=w.k, max_T=w.T, fmt=fmt)
             assert lay.kernel_name(w.T, "gate_up") == gu, (c, fmt)
             assert lay.kernel_name(w.T, "down") == dn, (c, fmt)
+            if c == 3:
+                # the warp-level MMA kernels when asked for
+                lay.close()
+                lay = MoEDecode(*device_weights(w, {}, dev, fmt=fmt), k=w.k, max_T=w.T, fmt=fmt,
+                                flags=MOE_FLAG_WARP_MMA)
+                assert lay.kernel_name(w.T, "gate_up") == "moe_gate_up_tma", fmt
+                assert lay.kernel_name(w.T, "down") == "moe_down_mma", fmt
             # the one-launch single-token form depends on the shape alone
             assert lay.fused_single_token == (c != 0), (c, fmt)
             lay.close()

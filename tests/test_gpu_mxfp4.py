@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_util import (Case, assert_within, bf16_tensor, device_weights, metrics, tensor_to_f64,
+from gpu_util import (Case, assert_within, bf16_tensor, check_layer_call, device_weights, metrics, tensor_to_f64,
                       tol_h, tol_y)
 from test_gpu_edges import Small, _layer_once
 
@@ -37,17 +37,12 @@ def _check_case(case: Case, dev, expect_fused=None):
     tw = torch.from_numpy(case.tw).to(dev)
     h = layer.gate_up(x, ids)
     y = layer.down(h, ids, tw)
-    y2 = layer.layer(x, ids, tw)
     torch.cuda.synchronize()
     ref = case.ref()
     S = case.tokens
     hm = assert_within(tensor_to_f64(h)[S], ref["h_spec"][S], tol_h(ref["h_spec"][S]), "h")
     ym = assert_within(tensor_to_f64(y)[S], ref["y_spec"][S], tol_y(ref["y_spec"][S]), "y")
-    if case.T == 1 and layer.fused_single_token:
-        assert_within(tensor_to_f64(y2)[S], ref["y_spec"][S], tol_y(ref["y_spec"][S]),
-                      "y (one launch)")
-    else:
-        assert torch.equal(y.view(torch.int16)[S], y2.view(torch.int16)[S])
+    check_layer_call(layer, case, x, ids, tw, y, fmt="mxfp4")
     assert layer.get_error() == 0
     layer.close()
     return hm, ym, metrics(tensor_to_f64(y)[S], ref["y_pure"][S])

@@ -12,8 +12,8 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_util import (Case, assert_within, bf16_tensor, device_weights, metrics, tensor_to_f64,
-                      tol_h, tol_y)
+from gpu_util import (Case, assert_within, bf16_tensor, check_layer_call, device_weights, metrics,
+                      tensor_to_f64, tol_h, tol_y)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,17 +41,12 @@ def _run_and_check(case: Case, dev, rows=None, expect_fused=None):
     tw = torch.from_numpy(case.tw).to(dev)
     h = layer.gate_up(x, ids)
     y = layer.down(h, ids, tw)
-    y2 = layer.layer(x, ids, tw)
     torch.cuda.synchronize()
     ref = case.ref()
     S = case.tokens
     hm = assert_within(tensor_to_f64(h)[S], ref["h_spec"][S], tol_h(ref["h_spec"][S]), "h")
     ym = assert_within(tensor_to_f64(y)[S], ref["y_spec"][S], tol_y(ref["y_spec"][S]), "y")
-    if case.T == 1 and layer.fused_single_token:
-        # one launch for both projections: its own sums, checked on their own
-        assert_within(tensor_to_f64(y2)[S], ref["y_spec"][S], tol_y(ref["y_spec"][S]), "y (one launch)")
-    else:
-        assert torch.equal(y.view(torch.int16)[S], y2.view(torch.int16)[S]), "layer() differs from gate_up+down"
+    check_layer_call(layer, case, x, ids, tw, y)
     pure = metrics(tensor_to_f64(y)[S], ref["y_pure"][S])
     assert layer.get_error() == 0
     layer.close()

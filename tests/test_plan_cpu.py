@@ -9,13 +9,13 @@ import itertools
 import pytest
 
 import workloads as wl
-from sparse_expert_gemv_gb300._lib import MOE_FLAG_MXFP4, MoEConfig, MoEPlan, lib
+from sparse_expert_gemv_gb300._lib import MOE_FLAG_MXFP4, MOE_FLAG_WARP_MMA, MoEConfig, MoEPlan, lib
 
 SMS, SMEM = 152, 232448          # GB300: SMs and opt-in shared memory per CTA
 
 
-def plan(E, k, H, I, T, fmt="mxfp8", sms=SMS, smem=SMEM):
-    cfg = MoEConfig(E, k, H, I, T, MOE_FLAG_MXFP4 if fmt == "mxfp4" else 0)
+def plan(E, k, H, I, T, fmt="mxfp8", sms=SMS, smem=SMEM, flags=0):
+    cfg = MoEConfig(E, k, H, I, T, (MOE_FLAG_MXFP4 if fmt == "mxfp4" else 0) | flags)
     out = MoEPlan()
     st = lib.moe_decode_plan(ctypes.byref(cfg), sms, smem, T, ctypes.byref(out))
     return st, out
@@ -31,14 +31,19 @@ def test_plan_rejects_what_create_rejects():
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
 def test_seeded_workloads(fmt):
-    want_gu = {0: 0, 1: 0, 2: 1, 3: 2, 4: 1}      # 0 L1, 1 x staged, 2 TMA + mma
-    want_dn = {0: 0, 1: 0, 2: 1, 3: 2, 4: 1}      # 0 warp per output, 1 TMA, 2 TMA + mma
+    # the warp path's kernels (workload 3's layer takes the tensor-core path
+    # when the weights allow it); with MOE_FLAG_WARP_MMA the 32-token
+    # workload's take the warp-level MMA
+    want_gu = {0: 0, 1: 0, 2: 1, 3: 1, 4: 1}      # 0 L1, 1 x staged, 2 TMA + mma
+    want_dn = {0: 0, 1: 0, 2: 1, 3: 1, 4: 1}      # 0 warp per output, 1 TMA, 2 TMA + mma
     for c, w in wl.WORKLOADS.items():
         st, p = plan(w.E, w.k, w.H, w.I, w.T, fmt)
         assert st == 0
         assert p.gate_up_kernel == want_gu[c], (c, fmt)
         assert p.down_kernel == want_dn[c], (c, fmt)
         assert p.fused == (0 if c == 0 else 1), (c, fmt)
+        st, p = plan(w.E, w.k, w.H, w.I, w.T, fmt, flags=MOE_FLAG_WARP_MMA)
+        assert (p.gate_up_kernel, p.down_kernel) == ((2, 2) if c == 3 else (want_gu[c], want_dn[c]))
     # the large-expert workload's gate/up runs as two groups of 8 tokens
     w = wl.workload(4)
     assert plan(w.E, w.k, w.H, w.I, w.T, fmt)[1].gate_up_group == 8
@@ -48,14 +53,17 @@ SHAPES = list(itertools.product([8, 128, 256], [1, 2, 8, 32], [256, 512, 1024, 2
                                 [32, 96, 128, 384, 768, 2048], [1, 2, 8, 16, 32, 40]))
 
 
+@pytest.mark.parametrize("mma", [False, True])
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
-def test_plan_invariants_over_shapes(fmt):
+def test_plan_invariants_over_shapes(fmt, mma):
     cb = 16 if fmt == "mxfp4" else 32               # code bytes per 32-element block
     n = 0
     for E, k, H, I, T in SHAPES:
         if k > E:
             continue
-        st, p = plan(E, k, H, I, T, fmt)
+        st, p = plan(E, k, H, I, T, fmt, flags=MOE_FLAG_WARP_MMA if mma else 0)
+        if not mma:
+            assert p.gate_up_kernel != 2 and p.down_kernel != 2
         assert st == 0
         n += 1
         if p.fused:
