@@ -119,6 +119,29 @@ __device__ __forceinline__ float dot_block(const uint8_t* codes, const uint8_t* 
   return (p + q) + (r + s);
 }
 
+// dot_block for two rows' codes (codes_a, codes_b) against one activation
+// block, whose chunks are read once.
+__device__ __forceinline__ void dot_block2(const uint8_t* codes_a, const uint8_t* codes_b,
+                                           const uint8_t* act, const LaneBlock& lb, float& da,
+                                           float& db) {
+  const uint4 x0 = *reinterpret_cast<const uint4*>(act + lb.x0);
+  const uint4 x1 = *reinterpret_cast<const uint4*>(act + lb.x1);
+  const uint4 x2 = *reinterpret_cast<const uint4*>(act + lb.x2);
+  const uint4 x3 = *reinterpret_cast<const uint4*>(act + lb.x3);
+  const uint4 a0 = *reinterpret_cast<const uint4*>(codes_a + lb.c_first);
+  const uint4 a1 = *reinterpret_cast<const uint4*>(codes_a + lb.c_second);
+  const uint4 b0 = *reinterpret_cast<const uint4*>(codes_b + lb.c_first);
+  const uint4 b1 = *reinterpret_cast<const uint4*>(codes_b + lb.c_second);
+  float p = 0.f, q = 0.f, r = 0.f, s = 0.f;
+  fma_e4m3x16(p, q, a0, x0, x1);
+  fma_e4m3x16(r, s, a1, x2, x3);
+  da = (p + q) + (r + s);
+  p = q = r = s = 0.f;
+  fma_e4m3x16(p, q, b0, x0, x1);
+  fma_e4m3x16(r, s, b1, x2, x3);
+  db = (p + q) + (r + s);
+}
+
 // Four E4M3 codes (one word) -> two f16x2 words: elements 0,1 and 2,3.
 __device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t codes, uint32_t& w01, uint32_t& w23) {
   asm("{\n\t.reg .b16 c0, c1;\n\tmov.b32 {c0, c1}, %2;\n\t"
@@ -158,6 +181,22 @@ __device__ __forceinline__ float dot_block_h(const uint32_t (&wh)[16], const uin
   const uint4 x1 = *reinterpret_cast<const uint4*>(act + lb.x1);
   const uint4 x2 = *reinterpret_cast<const uint4*>(act + lb.x2);
   const uint4 x3 = *reinterpret_cast<const uint4*>(act + lb.x3);
+  float p = 0.f, q = 0.f, r = 0.f, s = 0.f;
+  fma_f16x4(p, q, wh[0], wh[1], x0.x, x0.y);
+  fma_f16x4(p, q, wh[2], wh[3], x0.z, x0.w);
+  fma_f16x4(p, q, wh[4], wh[5], x1.x, x1.y);
+  fma_f16x4(p, q, wh[6], wh[7], x1.z, x1.w);
+  fma_f16x4(r, s, wh[8], wh[9], x2.x, x2.y);
+  fma_f16x4(r, s, wh[10], wh[11], x2.z, x2.w);
+  fma_f16x4(r, s, wh[12], wh[13], x3.x, x3.y);
+  fma_f16x4(r, s, wh[14], wh[15], x3.z, x3.w);
+  return (p + q) + (r + s);
+}
+
+// dot_block_h with the activation chunks already in registers (x0 .. x3 as
+// LaneBlock orders them: x0, x1 with wh[0..7], x2, x3 with wh[8..15]).
+__device__ __forceinline__ float dot_regs16(const uint32_t (&wh)[16], const uint4& x0,
+                                            const uint4& x1, const uint4& x2, const uint4& x3) {
   float p = 0.f, q = 0.f, r = 0.f, s = 0.f;
   fma_f16x4(p, q, wh[0], wh[1], x0.x, x0.y);
   fma_f16x4(p, q, wh[2], wh[3], x0.z, x0.w);
@@ -233,6 +272,11 @@ struct Mxfp8 {
                                                    const LaneBlock& lb) {
     return dot_block(codes, act, lb);
   }
+  __device__ __forceinline__ static void dot2_smem(const uint8_t* codes_a, const uint8_t* codes_b,
+                                                   const uint8_t* act, const LaneBlock& lb,
+                                                   float& da, float& db) {
+    dot_block2(codes_a, codes_b, act, lb, da, db);
+  }
   static constexpr int kLaneBytes = 8;
   static constexpr int kLaneWords = 2;
   __device__ __forceinline__ static void lds_lane(const uint8_t* p, uint32_t (&w)[kLaneWords]) {
@@ -278,6 +322,22 @@ struct Mxfp4 {
     uint32_t wh[16];
     decode(q, lb.c_first != 0, wh);
     return dot_block_h(wh, act, lb);
+  }
+  __device__ __forceinline__ static void dot2_smem(const uint8_t* codes_a, const uint8_t* codes_b,
+                                                   const uint8_t* act, const LaneBlock& lb,
+                                                   float& da, float& db) {
+    const uint4 x0 = *reinterpret_cast<const uint4*>(act + lb.x0);
+    const uint4 x1 = *reinterpret_cast<const uint4*>(act + lb.x1);
+    const uint4 x2 = *reinterpret_cast<const uint4*>(act + lb.x2);
+    const uint4 x3 = *reinterpret_cast<const uint4*>(act + lb.x3);
+    const uint4 a = *reinterpret_cast<const uint4*>(codes_a);
+    const uint4 b = *reinterpret_cast<const uint4*>(codes_b);
+    const uint32_t qa[4] = {a.x, a.y, a.z, a.w}, qb[4] = {b.x, b.y, b.z, b.w};
+    uint32_t wh[16];
+    decode(qa, lb.c_first != 0, wh);
+    da = dot_regs16(wh, x0, x1, x2, x3);
+    decode(qb, lb.c_first != 0, wh);
+    db = dot_regs16(wh, x0, x1, x2, x3);
   }
   static constexpr int kLaneBytes = 4;
   static constexpr int kLaneWords = 1;

@@ -571,35 +571,50 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
   named_sync(1, ncons);   // h staged
   if (ctid == 0) MOE_STAMP(MOE_TL_H_STAGED);
   {
-    const int wI = warp * IB, wS = warp * nbI;
+    // Row pairs over warps: warp w reduces rows q and q + np of the chunk
+    // (q = w mod np, np = half the chunk's rows, rounded up) against one
+    // half of the items (w / np), so each lane reads an item's h block once
+    // for two rows; the two halves' row sums are added in a fixed order.
+    float* red = reinterpret_cast<float*>(sm_words);   // [2][16]; the bitmaps are dead
     #pragma unroll 1
     while (have) {
-      float acc = 0.f;
-      if (warp < rc && !dead) {
+      const int np = (rc + 1) >> 1;
+      const int nh = kFusedConsumers / np >= 2 ? 2 : 1;
+      const int q = warp % np, hf = warp / np;
+      const int ra = q, rb = q + np < rc ? q + np : q;   // no second row: row q again
+      float acc_a = 0.f, acc_b = 0.f;
+      if (hf < nh && !dead) {
+        const int oa = ra * IB, ob = rb * IB, sa = ra * nbI, sb = rb * nbI;
 #pragma unroll 1
-        for (int t = lane; t < n_items; t += 64) {
-          // this item and the one 32 further on (the same one again past the end)
-          const bool two = t + 32 < n_items;
-          const int t2 = two ? t + 32 : t;
-          const float d1 = F::dot_smem(smem + tc[t] + wI, hs + 64 * t, lb);
-          const float d2 = F::dot_smem(smem + tc[t2] + wI, hs + 64 * t2, lb);
-          acc = fmaf(d1 * ue8m0_to_f32(smem[ts[t] + wS]), tf[t], acc);
-          if (two) acc = fmaf(d2 * ue8m0_to_f32(smem[ts[t2] + wS]), tf[t2], acc);
+        for (int t = lane + 32 * hf; t < n_items; t += 32 * nh) {
+          float da, db;
+          F::dot2_smem(smem + tc[t] + oa, smem + tc[t] + ob, hs + 64 * t, lb, da, db);
+          const float f = tf[t];
+          acc_a = fmaf(da * ue8m0_to_f32(smem[ts[t] + sa]), f, acc_a);
+          acc_b = fmaf(db * ue8m0_to_f32(smem[ts[t] + sb]), f, acc_b);
         }
       }
-      const float v = warp_sum(acc);
-      if (lane == 0 && warp < rc) p.y[c0 + warp] = f32_to_bf16_rn(v);
+      const float va = warp_sum(acc_a), vb = warp_sum(acc_b);
+      if (lane == 0 && hf < nh) {
+        red[hf * 16 + ra] = va;
+        if (q + np < rc) red[hf * 16 + q + np] = vb;
+      }
       // the chunk's slots are free again
       __syncwarp();
       RingPos r = pos0;
       for (int i = 0; i < ngr; ++i, r.next())
         if (lane == 0) mbar_arrive(&empty_g[r.slot]);
+      named_sync(1, ncons);   // every row sum is in red (and the item tables are read)
+      if (ctid < rc) {
+        float v = red[ctid];
+        if (nh == 2) v += red[16 + ctid];
+        p.y[c0 + ctid] = f32_to_bf16_rn(v);
+      }
       have = dw.valid;
       if (have) {
-        // every warp is past its reads of the item tables before they change
-        named_sync(1, ncons);
         chunk_tables();
         chunk_wait();
+        // the tables are ready, and red is read before it is written again
         named_sync(1, ncons);
       }
     }
