@@ -563,6 +563,7 @@ __global__ void __launch_bounds__(kTcGuThreads, 1) moe_tc_gate_up(const __grid_c
   if (warp == kTcWarpRaw) {
     if (lane == 0) {
       int gs = 0, gc = 0;
+      RingPos rw(R);   // the raw ring's slot and phase (no division by R per stage)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
         const int c = tile / MT, m = tile % MT;
@@ -578,13 +579,14 @@ __global__ void __launch_bounds__(kTcGuThreads, 1) moe_tc_gate_up(const __grid_c
             tma_load_2d(dst + kTcRows * 16, &p.tm_s, (s / kTcScaleStages) * 16, rg + I, &sc_full[slot]);
             ++gc;
           }
-          const int slot = gs % R;
-          if (gs >= R) ok = tc_wait(&raw_empty[slot], ((gs / R) - 1) & 1, p.err, dead);
+          const int slot = rw.slot;
+          if (gs >= R) ok = tc_wait(&raw_empty[slot], rw.phase ^ 1u, p.err, dead);
           if (!ok) break;
           uint8_t* dst = raw + slot * L.rawStage;
           mbar_expect_tx(&raw_full[slot], L.rawStage);
           tma_load_2d(dst, &p.tm_w, s * RB, rg, &raw_full[slot]);
           tma_load_2d(dst + kTcRows * RB, &p.tm_w, s * RB, rg + I, &raw_full[slot]);
+          rw.next();
         }
       }
       // never leave with copies in flight
@@ -690,6 +692,7 @@ __global__ void __launch_bounds__(kTcGuThreads, 1) moe_tc_gate_up(const __grid_c
     const int r = 32 * q + lane;                 // row among the tile's gate (or up) rows
     const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + kTcGuAcol + up * 32 + half * 16;
     int gs = 0, gc = 0;
+    RingPos rr(R);   // the raw ring's slot and phase (no division by R per stage)
     uint4 scw = make_uint4(0u, 0u, 0u, 0u);
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
@@ -703,13 +706,14 @@ __global__ void __launch_bounds__(kTcGuThreads, 1) moe_tc_gate_up(const __grid_c
           if (lane == 0) mbar_arrive(&sc_empty[slot]);
           ++gc;
         }
-        const int slot = gs % R;
-        ok = tc_wait_warp(&raw_full[slot], (gs / R) & 1, p.err, dead);
+        const int slot = rr.slot;
+        ok = tc_wait_warp(&raw_full[slot], rr.phase, p.err, dead);
         if (!ok) break;
         uint4 cc[2];
         F::load(raw + slot * L.rawStage + up * kTcRows * RB, r, half, cc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[slot]);
+        rr.next();
         const int bi = 2 * (s % kTcScaleStages) + half;   // block within the scale chunk
         const uint32_t word = bi < 4 ? scw.x : bi < 8 ? scw.y : bi < 12 ? scw.z : scw.w;
         uint32_t o[16];
@@ -807,6 +811,7 @@ __global__ void __launch_bounds__(kTcDnThreads, 1) moe_tc_down(const __grid_cons
   if (warp == kTcWarpRaw) {
     if (lane == 0) {
       int gs = 0, lt = 0;
+      RingPos rw(R);   // the raw ring's slot and phase (no division by R per stage)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++lt) {
         const int c = tile / MT, m = tile % MT;
@@ -817,11 +822,12 @@ __global__ void __launch_bounds__(kTcDnThreads, 1) moe_tc_down(const __grid_cons
         mbar_expect_tx(&sc_full[ss], kTcRows * nbI);
         bulk_copy_g2s(sc + ss * L.scStage, p.sd + row0 * nbI, kTcRows * nbI, &sc_full[ss]);
         for (int s = 0; s < nS; ++s, ++gs) {
-          const int slot = gs % R;
-          if (gs >= R) ok = tc_wait(&raw_empty[slot], ((gs / R) - 1) & 1, p.err, dead);
+          const int slot = rw.slot;
+          if (gs >= R) ok = tc_wait(&raw_empty[slot], rw.phase ^ 1u, p.err, dead);
           if (!ok) break;
           mbar_expect_tx(&raw_full[slot], L.rawStage);
           tma_load_2d(raw + slot * L.rawStage, &p.tm_w, s * RB, (int)row0, &raw_full[slot]);
+          rw.next();
         }
       }
       for (int d = gs - R < 0 ? 0 : gs - R; d < gs; ++d) mbar_wait(&raw_full[d % R], (d / R) & 1, p.err);
@@ -910,6 +916,7 @@ __global__ void __launch_bounds__(kTcDnThreads, 1) moe_tc_down(const __grid_cons
     const int r = 32 * q + lane;
     const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + kTcDnAcol + half * 16;
     int gs = 0, lt = 0;
+    RingPos rr(R);   // the raw ring's slot and phase (no division by R per stage)
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++lt) {
       const int ss = lt & 1;
@@ -917,14 +924,15 @@ __global__ void __launch_bounds__(kTcDnThreads, 1) moe_tc_down(const __grid_cons
       if (!ok) break;
       const uint8_t* srow = sc + ss * L.scStage + r * nbI;
       for (int s = 0; s < nS; ++s, ++gs) {
-        const int slot = gs % R;
-        ok = tc_wait_warp(&raw_full[slot], (gs / R) & 1, p.err, dead);
+        const int slot = rr.slot;
+        ok = tc_wait_warp(&raw_full[slot], rr.phase, p.err, dead);
         if (!ok) break;
         uint4 cc[2];
         F::load(raw + slot * L.rawStage, r, half, cc);
         const uint32_t sv = srow[2 * s + half];
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[slot]);
+        rr.next();
         uint32_t o[16];
         F::decode(cc, sv, o);
         const int as = gs % kTcDnSA;
