@@ -261,7 +261,11 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 template <int KMAX>
 struct WarpSchedule {
-  int id[KMAX];      // this lane's token's ids (-1: slot unused or invalid)
+  int id[KMAX];      // this lane's token's ids as loaded (dead after finish())
+  // the same after finish(), two to a word (slot j in bits 16 (j & 1) of word
+  // j / 2; 0xFFFF: slot unused or invalid), so that kernels holding the
+  // schedule through their main loop keep half the registers for it
+  uint32_t idp[(KMAX + 1) / 2];
   uint32_t badmask;  // slots j of this lane's token whose id is outside [0, E)
   uint32_t word;     // routed-expert bitmap word `lane`
   int excl;          // unique experts in words below `lane`
@@ -299,6 +303,12 @@ struct WarpSchedule {
       }
     }
     if (badmask) atomicOr(err, kDeviceBadId);
+#pragma unroll
+    for (int w = 0; w < (KMAX + 1) / 2; ++w) {
+      const uint32_t lo = id[2 * w] < 0 ? 0xFFFFu : (uint32_t)id[2 * w];
+      const uint32_t hi = 2 * w + 1 >= KMAX || id[2 * w + 1] < 0 ? 0xFFFFu : (uint32_t)id[2 * w + 1];
+      idp[w] = lo | (hi << 16);
+    }
     sm_words[lane] = 0u;
     __syncwarp();
 #pragma unroll
@@ -344,11 +354,17 @@ struct WarpSchedule {
     return (L & 31) * 32 + (int)__fns(w, 0, n + 1);
   }
 
+  // Slot j's id after finish() (-1: unused or invalid).
+  __device__ __forceinline__ int idj(int j) const {
+    const uint32_t v = (idp[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+    return v == 0xFFFFu ? -1 : (int)v;
+  }
+
   // Bits j of this lane's token whose id equals e.
   __device__ __forceinline__ uint32_t jmask(int e) const {
     uint32_t m = 0;
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) m |= (id[j] == e ? 1u : 0u) << j;
+    for (int j = 0; j < KMAX; ++j) m |= (idj(j) == e ? 1u : 0u) << j;
     return m;
   }
 };

@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) moe_layer_fused_t1(const __g
     float c = 0.f;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      const int idj = __shfl_sync(kFull, s.id[j], 0);    // lane 0 holds the token
+      const int idj = __shfl_sync(kFull, s.idj(j), 0);   // lane 0 holds the token
       const float wjj = __shfl_sync(kFull, wj, j);
       if (j < p.k && idj == e) {
         jm |= 1u << j;
