@@ -69,6 +69,7 @@ struct moe_decode {
   // pairs, its tensor maps (W_gateup codes and scales, W_down codes, xg, hg),
   // ring depths and shared-memory sizes
   bool tc_ok;
+  bool tc_f16_gu;                 // its gate/up weights decode exactly to f16 (moe_tc_gate_up<F, true>)
   int path;
   void* tc_mem;
   moe::TcWork tcw;
@@ -748,32 +749,37 @@ int tc_pairs(const moe_decode* m) { return std::min(m->cfg.max_T, moe::kTcMaxTok
 // Whether every weight decodes to a normal bf16 (scale codes in range, no
 // E4M3 NaN code): one pass over both projections' codes and scales. False
 // with ok = false when a CUDA call failed.
-bool tc_weights_exact(const moe_decode* m, bool& ok) {
+bool tc_weights_exact(moe_decode* m, bool& ok) {
   const moe_decode_config_t& c = m->cfg;
   const int CB = code_bytes_per_block(m);
   uint32_t* d = nullptr;
-  const uint32_t init[4] = {0xFFFFFFFFu, 0u, 0u, 0u};
-  uint32_t h[4] = {};
+  // gate/up's scale range and NaN flag, then down's
+  const uint32_t init[8] = {0xFFFFFFFFu, 0u, 0u, 0u, 0xFFFFFFFFu, 0u, 0u, 0u};
+  uint32_t h[8] = {};
   const size_t gu_scales = (size_t)c.E * 2 * c.I * (c.H / 32);
   const size_t dn_scales = (size_t)c.E * c.H * (c.I / 32);
   const size_t gu_codes = gu_scales * CB, dn_codes = dn_scales * CB;
   const dim3 grid(m->num_sms * 4), block(256);
   (void)cudaGetLastError();   // a launch error below must be this pass's own
-  ok = cudaMalloc(&d, 16) == cudaSuccess &&
-       cudaMemcpy(d, init, 16, cudaMemcpyHostToDevice) == cudaSuccess;
+  ok = cudaMalloc(&d, 32) == cudaSuccess &&
+       cudaMemcpy(d, init, 32, cudaMemcpyHostToDevice) == cudaSuccess;
   if (ok) {
     moe::moe_tc_scan<<<grid, block>>>(reinterpret_cast<const uint4*>(m->wgu), gu_codes / 16,
                                       reinterpret_cast<const uint4*>(m->sgu), gu_scales / 16,
                                       is_fp4(m) ? 0 : 1, d);
     moe::moe_tc_scan<<<grid, block>>>(reinterpret_cast<const uint4*>(m->wd), dn_codes / 16,
                                       reinterpret_cast<const uint4*>(m->sd), dn_scales / 16,
-                                      is_fp4(m) ? 0 : 1, d);
+                                      is_fp4(m) ? 0 : 1, d + 4);
     ok = cudaGetLastError() == cudaSuccess &&
-         cudaMemcpy(h, d, 16, cudaMemcpyDeviceToHost) == cudaSuccess;
+         cudaMemcpy(h, d, 32, cudaMemcpyDeviceToHost) == cudaSuccess;
   }
   if (d) cudaFree(d);
   const uint32_t lo = is_fp4(m) ? moe::kTcScaleMinFp4 : moe::kTcScaleMinFp8;
-  return ok && h[0] >= lo && h[1] <= (uint32_t)moe::kTcScaleMax && h[2] == 0u;
+  const uint32_t f16_hi = is_fp4(m) ? moe::kTcF16ScaleMaxFp4 : moe::kTcF16ScaleMaxFp8;
+  // the gate/up weights in f16 when their scale codes allow it
+  m->tc_f16_gu = ok && h[0] >= (uint32_t)moe::kTcF16ScaleMin && h[1] <= f16_hi && h[2] == 0u;
+  return ok && std::min(h[0], h[4]) >= lo && std::max(h[1], h[5]) <= (uint32_t)moe::kTcScaleMax &&
+         h[2] == 0u && h[6] == 0u;
 }
 
 // A [rows, cols] tensor of `dtype` (elem bytes each, rows `pitch` bytes
@@ -808,8 +814,11 @@ int tc_ring(const moe_decode* m, bool down, size_t& smem) {
 
 template <class F>
 cudaError_t set_tc_attributes(size_t gu, size_t dn, size_t prep) {
-  cudaError_t e = cudaFuncSetAttribute(moe::moe_tc_gate_up<F>,
+  cudaError_t e = cudaFuncSetAttribute(moe::moe_tc_gate_up<F, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gu);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(moe::moe_tc_gate_up<F, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gu);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(moe::moe_tc_down<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)dn);
@@ -842,9 +851,9 @@ bool tc_setup(moe_decode* m) {
   auto up256 = [](size_t v) { return (v + 255) / 256 * 256; };
   const size_t ints = up256((size_t)(4 + 3 * maxC + 2 * Pw) * 4);
   const size_t xg = up256((size_t)Pw * c.H * 2), hg = up256((size_t)Pw * c.I * 2);
-  const size_t yp = up256((size_t)Pw * c.H * 4);
-  if (cudaMalloc(&m->tc_mem, ints + xg + hg + yp) != cudaSuccess ||
-      cudaMemset(m->tc_mem, 0, ints + xg + hg + yp) != cudaSuccess)
+  const size_t yp = up256((size_t)Pw * c.H * 4), xi = up256((size_t)Pw * 4);
+  if (cudaMalloc(&m->tc_mem, ints + xg + hg + yp + xi) != cudaSuccess ||
+      cudaMemset(m->tc_mem, 0, ints + xg + hg + yp + xi) != cudaSuccess)
     return false;
   uint8_t* b = static_cast<uint8_t*>(m->tc_mem);
   int* iw = reinterpret_cast<int*>(b);
@@ -857,6 +866,7 @@ bool tc_setup(moe_decode* m) {
   m->tcw.xg = reinterpret_cast<uint16_t*>(b + ints);
   m->tcw.hg = reinterpret_cast<uint16_t*>(b + ints + xg);
   m->tcw.yp = reinterpret_cast<float*>(b + ints + xg + hg);
+  m->tcw.xinv = reinterpret_cast<float*>(b + ints + xg + hg + yp);
   const int CB = code_bytes_per_block(m);
   const int RB = is_fp4(m) ? moe::TcFp4::kStageRowBytes : moe::TcFp8::kStageRowBytes;
   const CUtensorMapSwizzle sw = is_fp4(m) ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -908,6 +918,7 @@ moe_status_t tc_layer_f(moe_decode* m, int T, const uint16_t* x, const int32_t* 
     pp.E = c.E;
     pp.H = c.H;
     pp.I = c.I;
+    pp.f16 = m->tc_f16_gu ? 1 : 0;
     moe::TcParams gp = {};
     gp.tm_w = m->tm_tc_gu;
     gp.tm_s = m->tm_tc_gus;
@@ -934,8 +945,11 @@ moe_status_t tc_layer_f(moe_decode* m, int T, const uint16_t* x, const int32_t* 
     const int G = m->num_sms;
     if (launch(moe::moe_tc_prep, dim3(std::min(G, P)), dim3(moe::kTcPrepThreads),
                moe::tc_prep_smem(P, c.E), s, pdl, pp) != cudaSuccess ||
-        launch(moe::moe_tc_gate_up<F>, dim3(G), dim3(moe::kTcGuThreads), m->tc_smem_gu, s, pdl,
-               gp) != cudaSuccess ||
+        (m->tc_f16_gu
+             ? launch(moe::moe_tc_gate_up<F, true>, dim3(G), dim3(moe::kTcGuThreads), m->tc_smem_gu,
+                      s, pdl, gp)
+             : launch(moe::moe_tc_gate_up<F, false>, dim3(G), dim3(moe::kTcGuThreads),
+                      m->tc_smem_gu, s, pdl, gp)) != cudaSuccess ||
         launch(moe::moe_tc_down<F>, dim3(G), dim3(moe::kTcDnThreads), m->tc_smem_dn, s, pdl,
                dp) != cudaSuccess ||
         launch(moe::moe_tc_combine, dim3((c.H + 4 * moe::kTcCombineThreads - 1) /

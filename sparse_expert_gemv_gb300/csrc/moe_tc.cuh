@@ -37,6 +37,7 @@
 #include <cstdint>
 
 #include "moe_device.cuh"
+#include "moe_f16blocks.cuh"
 
 namespace moe {
 
@@ -72,6 +73,13 @@ constexpr uint32_t kTcDnAcol = 128;
 constexpr int kTcScaleMinFp8 = 10;
 constexpr int kTcScaleMinFp4 = 2;
 constexpr int kTcScaleMax = 142;
+// gate/up scale codes for which every decoded weight is exact in f16 (E4M3
+// values are multiples of 2^-9 below 448, E2M1 values multiples of 2^-1 up
+// to 6; f16 holds multiples of 2^-24 below 65520, and the scale 2^(s-127)
+// itself is a normal f16 from s = 113)
+constexpr int kTcF16ScaleMin = 113;
+constexpr int kTcF16ScaleMaxFp8 = 134;
+constexpr int kTcF16ScaleMaxFp4 = 140;
 
 // Device views of the path's workspace (sized for kTcMaxTokens * k pairs).
 struct TcWork {
@@ -84,6 +92,7 @@ struct TcWork {
   uint16_t* xg;      // [pairs, H] bf16: x of each pair's token
   uint16_t* hg;      // [pairs, I] bf16: h of each pair
   float* yp;         // [pairs, H] FP32: W_down[e] h of each pair
+  float* xinv;       // [pairs] with an f16 xg: 2^-e of the pair's token's row
 };
 
 struct TcPrepParams {
@@ -93,6 +102,10 @@ struct TcPrepParams {
   uint32_t* err;
   TcWork w;
   int T, k, E, H, I;
+  // 0: xg holds x as is (bf16); 1: each row scaled by the power of two 2^e
+  // that brings its token's largest magnitude into [2^14, 2^15), in f16,
+  // with 2^-e in w.xinv
+  int f16;
 };
 
 struct TcParams {
@@ -155,10 +168,10 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
       : "memory");
 }
 
-// Instruction descriptor of kind::f16: FP32 D, bf16 A and B, both K-major,
-// M = 128, N = n (a multiple of 16, 16..256).
-__device__ __forceinline__ uint32_t idesc_bf16_m128(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+// Instruction descriptor of kind::f16: FP32 D, bf16 A and B (f16 A and B
+// when !bf16), both K-major, M = 128, N = n (a multiple of 16, 16..256).
+__device__ __forceinline__ uint32_t idesc_m128(int n, bool bf16) {
+  return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(kTcRows >> 4) << 24);
 }
 
@@ -263,6 +276,49 @@ __device__ __forceinline__ void decode_fp4_block(const uint4& a, uint32_t s, uin
   }
 }
 
+// f16 pair (2^(s-127), 2^(s-127)), for scale codes 113 <= s <= 142.
+__device__ __forceinline__ uint32_t scale_pair_f16(uint32_t s) {
+  return ((s - 112u) << 10) * 0x00010001u;
+}
+
+// 32 E4M3 codes -> 16 f16 pairs of code * 2^(s-127): the conversion, then one
+// f16 multiply a pair (exact for the scale codes kTcF16ScaleMin ..
+// kTcF16ScaleMaxFp8).
+__device__ __forceinline__ void decode_fp8_block_f16(const uint4& a, const uint4& b, uint32_t s,
+                                                     uint32_t (&o)[16]) {
+  const uint32_t f2 = scale_pair_f16(s);
+  const uint32_t q[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t lo, hi;
+    asm("{\n\t.reg .b16 u, v;\n\tmov.b32 {u, v}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, u;\n\tcvt.rn.f16x2.e4m3x2 %1, v;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(q[i]));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * i]) : "r"(lo), "r"(f2));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[2 * i + 1]) : "r"(hi), "r"(f2));
+  }
+}
+
+// 32 E2M1 codes -> 16 f16 pairs of code * 2^(s-127) (exact for the scale
+// codes kTcF16ScaleMin .. kTcF16ScaleMaxFp4).
+__device__ __forceinline__ void decode_fp4_block_f16(const uint4& a, uint32_t s,
+                                                     uint32_t (&o)[16]) {
+  const uint32_t f2 = scale_pair_f16(s);
+  const uint32_t q[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t w[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+        : "r"(q[i]));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[4 * i + j]) : "r"(w[j]), "r"(f2));
+  }
+}
+
 }  // namespace tc
 
 // The two weight formats as the tensor-core kernels read them: code bytes of
@@ -282,6 +338,10 @@ struct TcFp8 {
                                                 uint32_t (&o)[16]) {
     tc::decode_fp8_block(c[0], c[1], s, o);
   }
+  __device__ __forceinline__ static void decode_f16(const uint4 (&c)[2], uint32_t s,
+                                                    uint32_t (&o)[16]) {
+    tc::decode_fp8_block_f16(c[0], c[1], s, o);
+  }
 };
 struct TcFp4 {
   static constexpr int kStageRowBytes = 32;   // 32-byte swizzle: chunk c at c ^ ((r >> 2) & 1)
@@ -294,6 +354,10 @@ struct TcFp4 {
   __device__ __forceinline__ static void decode(const uint4 (&c)[2], uint32_t s,
                                                 uint32_t (&o)[16]) {
     tc::decode_fp4_block(c[0], s, o);
+  }
+  __device__ __forceinline__ static void decode_f16(const uint4 (&c)[2], uint32_t s,
+                                                    uint32_t (&o)[16]) {
+    tc::decode_fp4_block_f16(c[0], s, o);
   }
 };
 
@@ -424,11 +488,45 @@ __global__ void __launch_bounds__(kTcPrepThreads, 1) moe_tc_prep(const __grid_co
   // xg[q] = x[token of pair q] for pairs q = blockIdx.x, + gridDim.x, ...
   const int vpr = p.H / 8;   // 16-byte vectors a row
   const int rows = nP > (int)blockIdx.x ? (nP - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  for (int v = tid; v < rows * vpr; v += kTcPrepThreads) {
-    const int q = blockIdx.x + (v / vpr) * gridDim.x, c = v % vpr;
-    const int t = pslot[q] / p.k;
-    reinterpret_cast<uint4*>(p.w.xg + (size_t)q * p.H)[c] =
-        __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H) + c);
+  if (p.f16) {
+    // one warp a row: the token's largest magnitude, then the row in f16
+    // times the power of two 2^e that brings it into [2^14, 2^15) (as the
+    // warp kernels stage x, over the whole row here), and 2^-e
+    for (int r = warp; r < rows; r += NW) {
+      const int q = blockIdx.x + r * gridDim.x;
+      const int t = pslot[q] / p.k;
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H);
+      uint32_t m = 0;
+      for (int c = lane; c < vpr; c += 32) {
+        const uint4 v = __ldg(src + c);
+        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m = max(m, max(ww[i] & 0x7fffu, (ww[i] >> 16) & 0x7fffu));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
+      const int e = min(141 - (int)(m >> 7), 127);
+      const float up = exp2i(e);
+      for (int c = lane; c < vpr; c += 32) {
+        const uint4 v = __ldg(src + c);
+        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half2 hh = __floats2half2_rn(bf16_lo(ww[i]) * up, bf16_hi(ww[i]) * up);
+          o4[i] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+        reinterpret_cast<uint4*>(p.w.xg + (size_t)q * p.H)[c] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+      if (lane == 0) p.w.xinv[q] = exp2i(-e);
+    }
+  } else {
+    for (int v = tid; v < rows * vpr; v += kTcPrepThreads) {
+      const int q = blockIdx.x + (v / vpr) * gridDim.x, c = v % vpr;
+      const int t = pslot[q] / p.k;
+      reinterpret_cast<uint4*>(p.w.xg + (size_t)q * p.H)[c] =
+          __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H) + c);
+    }
   }
   // the caller's h slices of slots with invalid ids are zero
   if (bad) {
@@ -492,7 +590,10 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t* bar, uint32_t parity, uin
 // issues 2 x 4 MMAs (gate and up, K = 16 each) into the tile's accumulators.
 // Four epilogue warps turn a finished tile into h while the next one runs.
 // ---------------------------------------------------------------------------
-template <class F>
+// F16: the weights decode to f16 (scale codes in kTcF16ScaleMin ..
+// kTcF16ScaleMax*) against xg in f16 (per-token power-of-two scaling, undone
+// by w.xinv in the epilogue), else to bf16 against xg in bf16.
+template <class F, bool F16>
 __global__ void __launch_bounds__(kTcGuThreads, 1) moe_tc_gate_up(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
@@ -621,7 +722,7 @@ __global__ void __launch_bounds__(kTcGuThreads, 1) moe_tc_gate_up(const __grid_c
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++lt) {
         const int c = tile / MT;
         const int n16 = (p.w.chunk_n[c] + 15) & ~15;
-        const uint32_t idesc = tc::idesc_bf16_m128(n16);
+        const uint32_t idesc = tc::idesc_m128(n16, !F16);
         const int buf = lt & 1;
         if (lt >= 2) ok = tc_wait(&d_empty[buf], ((lt >> 1) - 1) & 1, p.err, dead);
         if (!ok) break;
@@ -669,11 +770,13 @@ __global__ void __launch_bounds__(kTcGuThreads, 1) moe_tc_gate_up(const __grid_c
         tc::ld16(lane_base + buf * 128 + 64 + c0, u);
         tc::wait_ld();
         const int myslot = (lane < 16 && c0 + lane < n) ? p.w.pair_slot[p0 + c0 + lane] : 0;
+        const float myinv = (F16 && lane < 16 && c0 + lane < n) ? p.w.xinv[p0 + c0 + lane] : 1.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int slot = __shfl_sync(kFull, myslot, j);
+          const float inv = F16 ? __shfl_sync(kFull, myinv, j) : 1.f;
           if (c0 + j < n) {
-            const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
+            const float gv = __uint_as_float(g[j]) * inv, uv = __uint_as_float(u[j]) * inv;
             const uint16_t hv = f32_to_bf16_rn((gv / (1.0f + expf(-gv))) * uv);
             p.w.hg[(size_t)(p0 + c0 + j) * I + i] = hv;
             p.h[(size_t)slot * I + i] = hv;
@@ -717,7 +820,10 @@ __global__ void __launch_bounds__(kTcGuThreads, 1) moe_tc_gate_up(const __grid_c
         const int bi = 2 * (s % kTcScaleStages) + half;   // block within the scale chunk
         const uint32_t word = bi < 4 ? scw.x : bi < 8 ? scw.y : bi < 12 ? scw.z : scw.w;
         uint32_t o[16];
-        F::decode(cc, (word >> (8 * (bi & 3))) & 0xFFu, o);
+        if constexpr (F16)
+          F::decode_f16(cc, (word >> (8 * (bi & 3))) & 0xFFu, o);
+        else
+          F::decode(cc, (word >> (8 * (bi & 3))) & 0xFFu, o);
         const int as = gs % kTcGuSA;
         if (gs >= kTcGuSA) ok = tc_wait_warp(&a_empty[as], ((gs / kTcGuSA) - 1) & 1, p.err, dead);
         if (!ok) break;
@@ -859,7 +965,7 @@ __global__ void __launch_bounds__(kTcDnThreads, 1) moe_tc_down(const __grid_cons
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x, ++lt) {
         const int c = tile / MT;
-        const uint32_t idesc = tc::idesc_bf16_m128((p.w.chunk_n[c] + 15) & ~15);
+        const uint32_t idesc = tc::idesc_m128((p.w.chunk_n[c] + 15) & ~15, true);
         const int buf = lt & 1;
         if (lt >= 2) ok = tc_wait(&d_empty[buf], ((lt >> 1) - 1) & 1, p.err, dead);
         if (!ok) break;

@@ -122,6 +122,19 @@ def test_same_result_twice_and_from_auto(dev):
     c.check(h3, y3)
 
 
+@pytest.mark.parametrize("fmt,sigma", [("mxfp8", 1e-7), ("mxfp8", 3e5), ("mxfp4", 1e-7),
+                                       ("mxfp4", 1.5e4)])
+def test_scales_outside_the_f16_range(sigma, fmt, dev):
+    # weights whose gate/up scale codes fall outside the range in which every
+    # weight is exact in f16 (113 .. 134 for MXFP8, 113 .. 140 for MXFP4) but
+    # inside the bf16 one (tiny: codes near 100; huge: 139 and 141): the
+    # gate/up kernel decodes them to bf16 instead, and the layer still
+    # matches the oracle
+    c = TcCase(dev, *SMALL, 64, seed=7, fmt=fmt, sigma=sigma)
+    assert c.layer.tensor_path
+    c.check(*c.run())
+
+
 def test_one_hot_expert_gets_every_token(dev):
     # every token routes slot 0 to expert 3: 200 pairs of one expert, four
     # column chunks (64 + 64 + 64 + 8)
