@@ -28,7 +28,9 @@ workload 1. --format mxfp4 stores the same weights as MXFP4 (E2M1 codes two
 to a byte, the same UE8M0 scales): half the code bytes per step.
 --tokens T runs the workload's layer at T tokens per step, and --path warp or
 tensor forces output-centric warp decode or the expert-centric tensor-core
-path (auto: the tensor-core path from 64 tokens) -- the crossover study. On
+path (auto: the tensor-core path from 16 tokens routing 1.5 or more slots per
+expert on average; warp-mma: warp decode whose 16- to 32-token calls use the
+warp-level MMA kernels, MOE_FLAG_WARP_MMA) -- the crossover study. On
 the tensor-core path the roofline line covers the whole step (its four
 launches against the step's weight bytes).
 """

@@ -264,7 +264,7 @@ int32_t moe_decode_fused_layer(moe_decode_t handle);
 /*
  * Which form moe_decode_layer and moe_decode_forward_host take:
  *   MOE_PATH_AUTO    (the default) the tensor-core path when the handle
- *                    supports it, T >= 16 and T * k >= 2 E (two or more
+ *                    supports it, T >= 16 and 2 T k >= 3 E (1.5 or more
  *                    routed slots per expert on average), output-centric
  *                    warp decode otherwise
  *   MOE_PATH_WARP    always warp decode (the one-launch kernel at T = 1)

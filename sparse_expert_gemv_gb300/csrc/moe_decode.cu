@@ -726,14 +726,13 @@ moe_status_t fused_layer(moe_decode* m, const uint16_t* x, const int32_t* ids, c
 // ---- expert-centric tensor-core path (moe_tc.cuh) --------------------------
 
 // MOE_PATH_AUTO takes the tensor-core path from kTcAutoMinTokens tokens when
-// they route at least kTcAutoSlotsPerExpert slots per expert on average.
+// they route at least 1.5 slots per expert on average (2 T k >= 3 E).
 // Measured on one GB300 (E = 128, k = 8, H = 2048, I = 768, MXFP8, us a
 // layer, FP32 warp kernels / tensor-core path): uniform routing T = 16
-// 132 / 196, T = 24 200 / 228, T = 32 246 / 249, T = 64 689 / 271; Zipf-skewed
-// routing T = 16 129 / 100, T = 32 231 / 111. E = 256 at T = 16 (one slot per
-// two experts): 916 / 1887.
+// 132 / 173, T = 24 200 / 201, T = 32 246 / 220, T = 64 689 (warp-level
+// MMA) / 239; Zipf-skewed routing T = 16 129 / 91, T = 24 179 / 97, T = 32
+// 231 / 100. E = 256 at T = 16 (one slot per two experts): 916 / 1631.
 constexpr int kTcAutoMinTokens = 16;
-constexpr int kTcAutoSlotsPerExpert = 2;
 
 // Shapes the path's kernels cover: whole 128-row tiles of I and H, gate/up
 // scale chunks of 512 elements, 16-byte aligned scale arrays, and TMA row
@@ -896,7 +895,7 @@ bool tc_setup(moe_decode* m) {
 bool use_tc(const moe_decode* m, int T) {
   if (!m->tc_ok || m->path == MOE_PATH_WARP) return false;
   return m->path == MOE_PATH_TENSOR ||
-         (T >= kTcAutoMinTokens && T * m->cfg.k >= kTcAutoSlotsPerExpert * m->cfg.E);
+         (T >= kTcAutoMinTokens && 2 * T * m->cfg.k >= 3 * m->cfg.E);
 }
 
 template <class F>

@@ -110,7 +110,7 @@ class MoEDecode:
 
     def set_path(self, path: str) -> None:
         """Which form layer calls take: "auto" (the tensor-core path from 16
-        tokens when they route two or more slots per expert on average),
+        tokens when they route 1.5 or more slots per expert on average),
         "warp" or "tensor"."""
         code = {"auto": MOE_PATH_AUTO, "warp": MOE_PATH_WARP, "tensor": MOE_PATH_TENSOR}[path]
         check(lib.moe_decode_set_path(self._h, code), "moe_decode_set_path")
