@@ -551,12 +551,13 @@ def run_ours(args, rank, world, local):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": 1e3 * dt_max / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if tensor else "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16/bf16" if tensor else "f32", "data": "synthetic",
             "config": {
                 "workload": w.name, "E": E, "k": k, "H": H, "I": I, "T": T,
                 "weights": ("MXFP4 (E2M1 two per byte + UE8M0 per 32)" if fmt == "mxfp4" else
                             "MXFP8 (E4M3 + UE8M0 per 32)")
-                           + (", decoded exactly to bf16, bf16 activations, tcgen05.mma with"
+                           + (", gate/up decoded exactly to f16 when every gate/up scale code"
+                              " keeps f16 exact (else bf16), down to bf16; tcgen05.mma with"
                               " FP32 accumulators" if tensor else
                               ", bf16 activations, FP32 accumulate")
                            + (" (random bytes generated on the device: timing only)" if big else ""),
