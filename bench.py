@@ -43,6 +43,7 @@ import json
 import multiprocessing
 import os
 import platform
+import re
 import statistics
 import subprocess
 import sys
@@ -115,13 +116,27 @@ def reduce_max(v, world):
     return float(t.item())
 
 
+# The files the one-launch kernel's device code and its launch come from: its
+# own header, the headers it includes, the host library and the C headers.
+FUSED_SOURCES = ("sparse_expert_gemv_gb300/csrc/moe_layer_fused.cuh",
+                 "sparse_expert_gemv_gb300/csrc/moe_kernels.cuh",
+                 "sparse_expert_gemv_gb300/csrc/moe_f16blocks.cuh",
+                 "sparse_expert_gemv_gb300/csrc/moe_device.cuh",
+                 "sparse_expert_gemv_gb300/csrc/moe_decode.cu",
+                 "include/moe_decode.h", "include/moe_decode_timeline.h")
+
+
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
 def source_hash() -> str:
-    """Hash of the CUDA sources the kernels are built from (a recorded ncu
-    traffic figure applies only while it matches)."""
+    """Hash of the code the one-launch kernel is built from, comments and
+    blank lines aside (its recorded ncu traffic figure applies only while
+    it matches)."""
     h = hashlib.sha256()
-    cdir = os.path.join(ROOT, "sparse_expert_gemv_gb300", "csrc")
-    for f in sorted(os.listdir(cdir)):
-        h.update(open(os.path.join(cdir, f), "rb").read())
+    for f in FUSED_SOURCES:
+        text = _COMMENT.sub("", open(os.path.join(ROOT, f)).read())
+        h.update("\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip()).encode())
     return h.hexdigest()[:16]
 
 

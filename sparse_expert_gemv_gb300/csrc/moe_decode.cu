@@ -128,6 +128,9 @@ int code_bytes_per_block(const moe_decode* m) { return is_fp4(m) ? 16 : 32; }
 constexpr uint32_t kKnownFlags =
     MOE_FLAG_NO_PDL | MOE_FLAG_HOST_COPY | MOE_FLAG_MXFP4 | MOE_FLAG_WARP_MMA;
 
+// The KMAX instance of the warp kernels for this handle's k (8 or 32).
+int kmax_of(const moe_decode* m) { return m->cfg.k <= 8 ? 8 : 32; }
+
 // Whether several-token warp-decode calls may take the warp-level MMA kernels.
 bool warp_mma(const moe_decode* m) { return (m->cfg.flags & MOE_FLAG_WARP_MMA) != 0; }
 
@@ -198,7 +201,7 @@ GuKind gate_up_kind(const moe_decode* m, int T, int& SG, size_t& smem) {
   }
   // several tokens whose x fits in shared memory: staged once per CTA as f16
   // blocks (one 16-warp CTA per SM)
-  smem = moe::gate_up_xs_smem(T, m->cfg.H);
+  smem = moe::gate_up_xs_smem(T, m->cfg.H, kmax_of(m));
   if (T >= 2 && smem <= m->smem_per_block) return GuKind::kXs;
   return GuKind::kL1;
 }
@@ -254,7 +257,12 @@ cudaError_t launch_gate_up(const moe_decode* m, const moe::GateUpParams& p, cuda
 
 // ---- down ------------------------------------------------------------------
 
-constexpr int kDownQ = 8;
+// Weight blocks a lane keeps in flight in moe_down_3d_batched: eight MXFP4
+// blocks (16 code bytes each) or six MXFP8 ones (32 bytes each), as many as
+// fit its 128 registers without spilling (a warp's 32 x 6 blocks still cover
+// the k I / 32 = 192 blocks of a 768-wide expert at k = 8 in one round).
+template <class F>
+constexpr int kDownQ = F::kBlockBytes == 16 ? 8 : 6;
 
 // Ring slots of moe_down_tma: as many as fit beside h (at most 16), 0 when
 // fewer than two fit.
@@ -334,7 +342,7 @@ DnKind down_kind(const moe_decode* m, int T, int& SG, size_t& smem) {
 int dn_mma_slots(const moe_decode* m, int T, size_t& smem) {
   const moe_decode_config_t& c = m->cfg;
   const int IB = c.I / 32 * code_bytes_per_block(m), nU_max = std::min(c.E, T * c.k);
-  auto bytes = [&](int SG) { return (size_t)moe::DmSmem(SG, c.I, IB, T, nU_max).total; };
+  auto bytes = [&](int SG) { return (size_t)moe::DmSmem(SG, c.I, IB, T, nU_max, kmax_of(m)).total; };
   if (bytes(2) > m->smem_per_block) return 0;
   int SG = 2;
   while (SG < moe::kDmConsumers && bytes(SG + 1) <= m->smem_per_block) ++SG;
@@ -390,8 +398,8 @@ cudaError_t launch_down(const moe_decode* m, const moe::DownParams& p, cudaStrea
                      : launch_down_tma<moe::Mxfp8>(m, p, SG, smem, s);
   const dim3 grid(p.H / moe::kWarps, p.T), block(moe::kThreads);
   if (is_fp4(m))
-    return launch(moe::moe_down_3d_batched<kDownQ, moe::Mxfp4>, grid, block, smem, s, use_pdl(m), p);
-  return launch(moe::moe_down_3d_batched<kDownQ, moe::Mxfp8>, grid, block, smem, s, use_pdl(m), p);
+    return launch(moe::moe_down_3d_batched<kDownQ<moe::Mxfp4>, moe::Mxfp4>, grid, block, smem, s, use_pdl(m), p);
+  return launch(moe::moe_down_3d_batched<kDownQ<moe::Mxfp8>, moe::Mxfp8>, grid, block, smem, s, use_pdl(m), p);
 }
 
 // The down kernels' shared-memory limit: one value for every handle, the
@@ -409,8 +417,8 @@ cudaError_t set_down_attributes() {
                         (const void*)moe::moe_down_mma<8, moe::Mxfp4>,
                         (const void*)moe::moe_down_mma<32, moe::Mxfp4>})
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-  for (const void* f : {(const void*)moe::moe_down_3d_batched<kDownQ, moe::Mxfp8>,
-                        (const void*)moe::moe_down_3d_batched<kDownQ, moe::Mxfp4>})
+  for (const void* f : {(const void*)moe::moe_down_3d_batched<kDownQ<moe::Mxfp8>, moe::Mxfp8>,
+                        (const void*)moe::moe_down_3d_batched<kDownQ<moe::Mxfp4>, moe::Mxfp4>})
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDownSmem);
   return e;
@@ -729,9 +737,9 @@ moe_status_t fused_layer(moe_decode* m, const uint16_t* x, const int32_t* ids, c
 // they route at least 1.5 slots per expert on average (2 T k >= 3 E).
 // Measured on one GB300 (E = 128, k = 8, H = 2048, I = 768, MXFP8, us a
 // layer, FP32 warp kernels / tensor-core path): uniform routing T = 16
-// 132 / 173, T = 24 200 / 201, T = 32 246 / 220, T = 64 689 (warp-level
-// MMA) / 239; Zipf-skewed routing T = 16 129 / 91, T = 24 179 / 97, T = 32
-// 231 / 100. E = 256 at T = 16 (one slot per two experts): 916 / 1631.
+// 132 / 154, T = 24 192 / 178, T = 32 238 / 194; Zipf-skewed routing
+// T = 16 128 / 82, T = 24 178 / 88, T = 32 232 / 91. E = 256 at T = 16 (one
+// slot per two experts): 916 / 1412.
 constexpr int kTcAutoMinTokens = 16;
 
 // Shapes the path's kernels cover: whole 128-row tiles of I and H, gate/up
@@ -979,8 +987,8 @@ int gate_up_group(const moe_decode* m, int T) {
   size_t smem = 0;
   if (g < 2 || gate_up_kind(m, g, SG, smem) != GuKind::kL1) return g;
   int g2 = g;
-  while (g2 > 4 && moe::gate_up_xs_smem(g2, m->cfg.H) > m->smem_per_block) --g2;
-  if (moe::gate_up_xs_smem(g2, m->cfg.H) > m->smem_per_block) return g;
+  while (g2 > 4 && moe::gate_up_xs_smem(g2, m->cfg.H, kmax_of(m)) > m->smem_per_block) --g2;
+  if (moe::gate_up_xs_smem(g2, m->cfg.H, kmax_of(m)) > m->smem_per_block) return g;
   // equal groups: T = 16 with room for 15 runs as two groups of 8
   const int n = (T + g2 - 1) / g2;
   return (T + n - 1) / n;

@@ -237,6 +237,50 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// The tokens of one pass over a unit's rows: the lowest NT set bits of the
+// unit's token mask (grp holds them only for groups kept as a mask). Groups of up to four keep the token indices in
+// registers; larger groups keep only the mask and walk it where a token is
+// needed, leaving their NT registers to the accumulators.
+template <int NT>
+struct TokenGroup {
+  static constexpr bool kMask = NT > 4;
+  int tok[kMask ? 1 : NT];
+  uint32_t grp;   // the group's tokens
+  int nt;         // how many (<= NT)
+  // Takes the group from `tokens` (removing it there).
+  __device__ __forceinline__ void take(uint32_t& tokens) {
+    if constexpr (kMask) {
+      uint32_t rest = tokens;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) rest &= rest - 1;   // drop the lowest NT
+      grp = tokens ^ rest;
+      nt = __popc(grp);
+      tokens = rest;
+    } else {
+      grp = 0u;
+      nt = 0;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        tok[n] = tokens ? __ffs(tokens) - 1 : 0;
+        if (tokens) {
+          tokens &= tokens - 1;
+          ++nt;
+        }
+      }
+    }
+  }
+  // Token n of the group, for n = 0, 1, ... in order; `walk` starts at grp.
+  __device__ __forceinline__ int token(int n, uint32_t& walk) const {
+    if constexpr (kMask) {
+      const int t = __ffs(walk) - 1;
+      walk &= walk - 1;
+      return t;
+    } else {
+      return tok[n];
+    }
+  }
+};
+
 // ---------------------------------------------------------------------------
 // programmatic dependent launch
 // ---------------------------------------------------------------------------
@@ -255,26 +299,49 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // over E (word w held by lane w, E <= 1024); its popcount prefix numbers the
 // unique experts in ascending id order. For a given expert, each lane reports
 // which of its slots j route there (jmask), and a ballot gives the tokens.
-// Everything lives in registers plus 32 words of per-warp shared memory, so
-// each warp builds it alone with no block barrier.
+// Everything lives in registers plus per-warp shared memory (32 bitmap words,
+// and with IdStore::kShared the packed ids), so each warp builds it alone
+// with no block barrier.
 // ---------------------------------------------------------------------------
 
-template <int KMAX>
+// Where a schedule keeps its lanes' ids after finish(): in registers, or in
+// a [(KMAX + 1) / 2][32]-word table of the warp's shared memory (lane-minor,
+// so a lane's reads are conflict-free), which gives the registers back to
+// kernels that hold many tokens' accumulators through their main loop.
+enum class IdStore { kRegisters, kShared };
+
+// Shared-memory bytes of one warp's id table for IdStore::kShared.
+__host__ __device__ constexpr int schedule_id_bytes(int kmax) { return (kmax + 1) / 2 * 32 * 4; }
+
+// The several-token warp kernels keep a token's ids in registers when there
+// are at most eight slots and the kernel holds at most two tokens'
+// accumulators at a time, else in shared memory (where registers would
+// spill).
+template <int NT, int KMAX>
+constexpr IdStore kWarpIdStore = KMAX > 8 || NT > 2 ? IdStore::kShared : IdStore::kRegisters;
+
+template <int KMAX, IdStore S = IdStore::kRegisters>
 struct WarpSchedule {
+  static constexpr int kIdWords = (KMAX + 1) / 2;
+  static constexpr bool kShared = S == IdStore::kShared;
   int id[KMAX];      // this lane's token's ids as loaded (dead after finish())
   // the same after finish(), two to a word (slot j in bits 16 (j & 1) of word
-  // j / 2; 0xFFFF: slot unused or invalid), so that kernels holding the
-  // schedule through their main loop keep half the registers for it
-  uint32_t idp[(KMAX + 1) / 2];
+  // j / 2; 0xFFFF: slot unused or invalid): in registers, or in word j / 2 of
+  // this lane's column of the warp's shared table
+  uint32_t idp[kShared ? 1 : kIdWords];
+  uint32_t* idcol;   // IdStore::kShared: this lane's column (stride 32 words)
   uint32_t badmask;  // slots j of this lane's token whose id is outside [0, E)
   uint32_t word;     // routed-expert bitmap word `lane`
   int excl;          // unique experts in words below `lane`
   int n_unique;
 
+  // sm_ids: the warp's id table (schedule_id_bytes(KMAX) bytes) with
+  // IdStore::kShared, unused otherwise.
   __device__ __forceinline__ void build(const int32_t* __restrict__ ids, int T, int k, int E,
-                                        uint32_t* sm_words, uint32_t* err) {
+                                        uint32_t* sm_words, uint32_t* err,
+                                        uint32_t* sm_ids = nullptr) {
     load(ids, T, k);
-    finish(E, sm_words, err);
+    finish(E, sm_words, err, sm_ids);
   }
 
   // The two halves of build(): load() only issues the id loads, so that
@@ -291,7 +358,8 @@ struct WarpSchedule {
       }
     }
   }
-  __device__ __forceinline__ void finish(int E, uint32_t* sm_words, uint32_t* err) {
+  __device__ __forceinline__ void finish(int E, uint32_t* sm_words, uint32_t* err,
+                                         uint32_t* sm_ids = nullptr) {
     const int lane = threadIdx.x & 31;
     const uint32_t used = badmask;
     badmask = 0u;
@@ -303,11 +371,15 @@ struct WarpSchedule {
       }
     }
     if (badmask) atomicOr(err, kDeviceBadId);
+    if constexpr (kShared) idcol = sm_ids + lane;
 #pragma unroll
-    for (int w = 0; w < (KMAX + 1) / 2; ++w) {
+    for (int w = 0; w < kIdWords; ++w) {
       const uint32_t lo = id[2 * w] < 0 ? 0xFFFFu : (uint32_t)id[2 * w];
       const uint32_t hi = 2 * w + 1 >= KMAX || id[2 * w + 1] < 0 ? 0xFFFFu : (uint32_t)id[2 * w + 1];
-      idp[w] = lo | (hi << 16);
+      if constexpr (kShared)
+        idcol[32 * w] = lo | (hi << 16);
+      else
+        idp[w] = lo | (hi << 16);
     }
     sm_words[lane] = 0u;
     __syncwarp();
@@ -356,15 +428,30 @@ struct WarpSchedule {
 
   // Slot j's id after finish() (-1: unused or invalid).
   __device__ __forceinline__ int idj(int j) const {
-    const uint32_t v = (idp[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+    uint32_t wd;
+    if constexpr (kShared)
+      wd = idcol[32 * (j >> 1)];
+    else
+      wd = idp[j >> 1];
+    const uint32_t v = (wd >> (16 * (j & 1))) & 0xFFFFu;
     return v == 0xFFFFu ? -1 : (int)v;
   }
 
   // Bits j of this lane's token whose id equals e.
   __device__ __forceinline__ uint32_t jmask(int e) const {
     uint32_t m = 0;
+    if constexpr (kShared) {
+      // one shared load per two slots (e is a valid id, never 0xFFFF)
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) m |= (idj(j) == e ? 1u : 0u) << j;
+      for (int w = 0; w < kIdWords; ++w) {
+        const uint32_t wd = idcol[32 * w];
+        m |= ((wd & 0xFFFFu) == (uint32_t)e ? 1u : 0u) << (2 * w);
+        if (2 * w + 1 < KMAX) m |= ((wd >> 16) == (uint32_t)e ? 1u : 0u) << (2 * w + 1);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) m |= (idj(j) == e ? 1u : 0u) << j;
+    }
     return m;
   }
 };

@@ -63,11 +63,12 @@ __host__ __device__ constexpr int dm_hrow(int I) { return I * 2 + 16; }
 
 // Shared-memory map (byte offsets, 128-byte aligned): the ring (slot = 16
 // rows of codes, their scales, eight h rows), each consumer warp's y
-// accumulator [T][16], the mbarriers, the warps' schedule words, each warp's
-// column list, and the item prefixes.
+// accumulator [T][16], the mbarriers, the warps' schedule words and id
+// tables (KMAX slots a token), each warp's column list, the item prefixes,
+// and the tokens' routing weights [T][k].
 struct DmSmem {
-  int codes, hsl, slot, yacc, bars, words, tl, pref, total;
-  __host__ __device__ DmSmem(int SG, int I, int IB, int T, int nU_max) {
+  int codes, hsl, slot, yacc, bars, words, ids, tl, pref, wts, total;
+  __host__ __device__ DmSmem(int SG, int I, int IB, int T, int nU_max, int kmax) {
     codes = kDmRows * IB;
     hsl = round128(kDmRows * IB + kDmRows * (I >> 5));
     slot = round128(hsl + kDmTokens * dm_hrow(I));
@@ -78,10 +79,14 @@ struct DmSmem {
     o += round128(2 * SG * 8);
     words = o;
     o += (kDmConsumers + 1) * 32 * 4;
+    ids = o;
+    o += (kDmConsumers + 1) * schedule_id_bytes(kmax);
     tl = o;
     o += (kDmConsumers + 1) * 3 * kDmTokens * 4;
     pref = o;
     o += round128((nU_max + 1) * 4);
+    wts = o;
+    o += round128(T * kmax * 4);
     total = o;
   }
 };
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(kDmThreads, 1) moe_down_mma(const __grid_const
   const int H = p.H, I = p.I, k = p.k, SG = p.SG, nbI = I >> 5, IB = nbI * CB;
   const int hrow = dm_hrow(I);
   const int nU_max = min(p.E, p.T * k);
-  const DmSmem L(SG, I, IB, p.T, nU_max);
+  const DmSmem L(SG, I, IB, p.T, nU_max, KMAX);
   uint8_t* ring = smem;
   float* yacc = reinterpret_cast<float*>(smem + L.yacc);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
@@ -138,9 +143,13 @@ __global__ void __launch_bounds__(kDmThreads, 1) moe_down_mma(const __grid_const
   }
   pdl_wait();      // h comes from the gate/up kernel, ids and w from upstream work
   pdl_trigger();
-  WarpSchedule<KMAX> s;
-  s.build(p.ids, p.T, k, p.E, sm_words + warp * 32, p.err);
+  WarpSchedule<KMAX, IdStore::kShared> s;
+  s.build(p.ids, p.T, k, p.E, sm_words + warp * 32, p.err,
+          reinterpret_cast<uint32_t*>(smem + L.ids + warp * schedule_id_bytes(KMAX)));
   const int nU = s.n_unique;
+  // the tokens' routing weights, read once per CTA
+  float* wts = reinterpret_cast<float*>(smem + L.wts);
+  for (int i = threadIdx.x; i < p.T * k; i += kDmThreads) wts[i] = __ldg(p.w + i);
   // passes of each unique expert (its tokens in groups of eight)
 #pragma unroll 1
   for (int u = warp; u < nU; u += kDmConsumers + 1) {
@@ -171,11 +180,6 @@ __global__ void __launch_bounds__(kDmThreads, 1) moe_down_mma(const __grid_const
   int* tl = reinterpret_cast<int*>(smem + L.tl) + warp * 3 * kDmTokens;
   int* tjf = tl + kDmTokens;
   float* tw = reinterpret_cast<float*>(tl + 2 * kDmTokens);
-  // lane t: token t's routing weights, loaded once
-  float wreg[KMAX];
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j)
-    wreg[j] = (lane < p.T && j < k) ? __ldg(p.w + (size_t)lane * k + j) : 0.f;
 
   // The walk over items (expert u, pass) of each tile, shared by producer and
   // consumers: the columns of an item are tokens base .. base+nt-1 of the
@@ -187,10 +191,8 @@ __global__ void __launch_bounds__(kDmThreads, 1) moe_down_mma(const __grid_const
     const int base = kDmTokens * pass;
     nt = min(kDmTokens, __popc(tokens) - base);
     const int rank = __popc(tokens & ((1u << lane) - 1u)) - base;
-    float cw = 0.f;
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j)
-      if ((jm >> j) & 1u) cw += wreg[j];
+    float cw = 0.f;   // token `lane`'s weights of its slots on e, in slot order
+    for (uint32_t m = jm; m; m &= m - 1) cw += wts[lane * k + __ffs(m) - 1];
     __syncwarp();
     if (jm != 0u && rank >= 0 && rank < kDmTokens) {
       tl[rank] = lane;
@@ -269,6 +271,9 @@ __global__ void __launch_bounds__(kDmThreads, 1) moe_down_mma(const __grid_const
       const uint32_t phase = (uint32_t)((qi / SG) & 1);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       if (!dead) dead = !mbar_wait(&full[slot], phase, p.err);
+      // the shuffles and MMAs below need the whole warp: a wait that ran out
+      // on any lane stops them on every lane
+      dead = __any_sync(kFull, dead);
       if (!dead) {
         const uint8_t* st = ring + (size_t)slot * L.slot;
         const uint8_t* hb = st + L.hsl + g * hrow + 16 * c;

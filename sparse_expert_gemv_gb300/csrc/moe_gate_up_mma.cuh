@@ -346,6 +346,9 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gate_up_tma(const __grid_co
 #pragma unroll 1
     for (int kc = 0; kc < nkc; ++kc, rg.next()) {
       if (!dead) dead = !mbar_wait(&full[rg.slot], rg.phase, p.err);
+      // the MMAs below need the whole warp: a wait that ran out on any lane
+      // stops them on every lane
+      dead = __any_sync(kFull, dead);
       if (!dead) {
         const uint8_t* st = ring + (size_t)rg.slot * L.slot;
         const uint8_t* ss = sring + (size_t)rg.slot * L.sslot;

@@ -91,11 +91,12 @@ __global__ void __launch_bounds__(32) moe_dedup_schedule_kernel(const int32_t* _
                                                                 int32_t* pairs, int32_t* n_uniq,
                                                                 uint32_t* err) {
   __shared__ uint32_t sm_words[32];
+  __shared__ uint32_t sm_ids[schedule_id_bytes(KMAX) / 4];
   const int lane = threadIdx.x & 31;
   pdl_wait();
   pdl_trigger();
-  WarpSchedule<KMAX> s;
-  s.build(ids, T, k, E, sm_words, err);
+  WarpSchedule<KMAX, IdStore::kShared> s;
+  s.build(ids, T, k, E, sm_words, err, sm_ids);
   int base = 0;
   for (int u = 0; u < s.n_unique; ++u) {
     const int e = s.expert(u);
@@ -146,7 +147,7 @@ template <int NT, class F>
 __device__ __forceinline__ void gate_up_block(const uint32_t (&qg)[F::kWords],
                                               const uint32_t (&qu)[F::kWords], float scg,
                                               float scu, const uint16_t* __restrict__ x,
-                                              const int (&tok)[NT], int nt, int H, int b,
+                                              const TokenGroup<NT>& tg, int H, int b,
                                               float (&ag)[NT], float (&au)[NT]) {
   float pg[NT], pu[NT];
 #pragma unroll
@@ -156,10 +157,11 @@ __device__ __forceinline__ void gate_up_block(const uint32_t (&qg)[F::kWords],
     float g[8], u[8];
     F::chunk_f32(qg, c, g);
     F::chunk_f32(qu, c, u);
+    uint32_t gm = tg.grp;
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-      if (n < nt) {
-        const uint4 xv = ld_act16(x + (size_t)tok[n] * H + b * 32 + c * 8);
+      if (n < tg.nt) {
+        const uint4 xv = ld_act16(x + (size_t)tg.token(n, gm) * H + b * 32 + c * 8);
         const float xs[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
                              bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
 #pragma unroll
@@ -180,12 +182,14 @@ __device__ __forceinline__ void gate_up_block(const uint32_t (&qg)[F::kWords],
 template <int NT, int KMAX, class F>
 __global__ void __launch_bounds__(kThreads, 2) moe_gate_up_3d_batched(GateUpParams p) {
   __shared__ uint32_t sm_words[kWarps][32];
+  constexpr IdStore kIds = kWarpIdStore<NT, KMAX>;
+  __shared__ uint32_t sm_ids[kWarps][kIds == IdStore::kShared ? schedule_id_bytes(KMAX) / 4 : 1];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   pdl_wait();      // x and topk_ids come from upstream work
   pdl_trigger();   // the down kernel may start fetching its weights
-  WarpSchedule<KMAX> s;
-  s.build(p.ids, p.T, p.k, p.E, sm_words[wid], p.err);
+  WarpSchedule<KMAX, kIds> s;
+  s.build(p.ids, p.T, p.k, p.E, sm_words[wid], p.err, sm_ids[wid]);
   const int H = p.H, I = p.I, nb = H >> 5;
   // A slot with an out-of-range id gets no unit; its h slice is defined as zero.
   if (__any_sync(kFull, s.badmask != 0u)) {
@@ -213,16 +217,9 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gate_up_3d_batched(GateUpPara
     const uint8_t* sg = p.sgu + row * nb;
     const uint8_t* su = sg + (size_t)I * nb;
     while (tokens) {
-      int tok[NT];
-      int nt = 0;
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        tok[n] = tokens ? __ffs(tokens) - 1 : 0;
-        if (tokens) {
-          tokens &= tokens - 1;
-          ++nt;
-        }
-      }
+      TokenGroup<NT> tg;   // this pass's tokens: the lowest NT of `tokens`
+      tg.take(tokens);
+      const int nt = tg.nt;
       float ag[NT], au[NT];
 #pragma unroll
       for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
@@ -244,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gate_up_3d_batched(GateUpPara
           s1g = ld_scale(sg + b1);
           s1u = ld_scale(su + b1);
         }
-        gate_up_block<NT, F>(qg0, qu0, ue8m0_to_f32(s0g), ue8m0_to_f32(s0u), p.x, tok, nt, H, b,
+        gate_up_block<NT, F>(qg0, qu0, ue8m0_to_f32(s0g), ue8m0_to_f32(s0u), p.x, tg, H, b,
                              ag, au);
         if (b1 >= nb) break;
         const int b2 = b1 + 32;
@@ -254,19 +251,21 @@ __global__ void __launch_bounds__(kThreads, 2) moe_gate_up_3d_batched(GateUpPara
           s0g = ld_scale(sg + b2);
           s0u = ld_scale(su + b2);
         }
-        gate_up_block<NT, F>(qg1, qu1, ue8m0_to_f32(s1g), ue8m0_to_f32(s1u), p.x, tok, nt, H, b1,
+        gate_up_block<NT, F>(qg1, qu1, ue8m0_to_f32(s1g), ue8m0_to_f32(s1u), p.x, tg, H, b1,
                              ag, au);
         b = b2;
       }
+      uint32_t gm = tg.grp;
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         if (n < nt) {
+          const int t = tg.token(n, gm);
           const float g = warp_sum(ag[n]);
           const float up = warp_sum(au[n]);
-          const uint32_t jt = __shfl_sync(kFull, jm, tok[n]);
+          const uint32_t jt = __shfl_sync(kFull, jm, t);
           const float hv = (g / (1.0f + expf(-g))) * up;
           const uint16_t hb = f32_to_bf16_rn(hv);
-          if (lane < p.k && ((jt >> lane) & 1u)) p.h[((size_t)tok[n] * p.k + lane) * I + i] = hb;
+          if (lane < p.k && ((jt >> lane) & 1u)) p.h[((size_t)t * p.k + lane) * I + i] = hb;
         }
       }
     }
@@ -336,10 +335,15 @@ __device__ __forceinline__ void down_load_round(const DownParams& p, int f0, int
 constexpr int kXsWarps = 16;
 constexpr int kXsThreads = kXsWarps * 32;
 
-// Shared-memory bytes of moe_gate_up_3d_batched_xs for T tokens of H (all of it dynamic:
-// the warps' schedule words, then x as f16 blocks, then their factors).
-__host__ __device__ constexpr size_t gate_up_xs_smem(int T, int H) {
-  return (size_t)kXsWarps * 32 * 4 + (size_t)T * (H >> 5) * (64 + 4);
+// Shared-memory bytes of moe_gate_up_3d_batched_xs for T tokens of H and
+// KMAX slots a token (all of it dynamic: the warps' schedule words and id
+// tables, then x as f16 blocks, then their factors).
+__host__ __device__ constexpr size_t gate_up_xs_ids_offset() { return (size_t)kXsWarps * 32 * 4; }
+__host__ __device__ constexpr size_t gate_up_xs_x_offset(int kmax) {
+  return gate_up_xs_ids_offset() + (size_t)kXsWarps * schedule_id_bytes(kmax);
+}
+__host__ __device__ constexpr size_t gate_up_xs_smem(int T, int H, int kmax) {
+  return gate_up_xs_x_offset(kmax) + (size_t)T * (H >> 5) * (64 + 4);
 }
 
 // D: weight blocks per lane in flight (1, or 2 when registers allow).
@@ -350,11 +354,12 @@ __global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_3d_batched_xs(GateU
   const int wid = threadIdx.x >> 5;
   const int H = p.H, I = p.I, nb = H >> 5;
   uint32_t* sm_words = reinterpret_cast<uint32_t*>(smem);              // [warps][32]
-  uint8_t* xs = smem + kXsWarps * 32 * 4;                              // [T][nb] x blocks
+  uint32_t* sm_ids = reinterpret_cast<uint32_t*>(smem + gate_up_xs_ids_offset());
+  uint8_t* xs = smem + gate_up_xs_x_offset(KMAX);                      // [T][nb] x blocks
   float* xf = reinterpret_cast<float*>(xs + (size_t)p.T * nb * 64);    // [T][nb] factors
   pdl_wait();      // x and topk_ids come from upstream work
   pdl_trigger();   // the down kernel may start fetching its weights
-  WarpSchedule<KMAX> s;
+  WarpSchedule<KMAX, kWarpIdStore<NT, KMAX>> s;   // (the id tables are reserved either way)
   s.load(p.ids, p.T, p.k);
   // x -> f16 blocks while the ids are in flight
 #pragma unroll 1
@@ -364,7 +369,7 @@ __global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_3d_batched_xs(GateU
     const uint4 v[4] = {__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3)};
     xf[idx] = stage_block_f16(v, xs + 64 * idx, b);
   }
-  s.finish(p.E, sm_words + wid * 32, p.err);
+  s.finish(p.E, sm_words + wid * 32, p.err, sm_ids + wid * (schedule_id_bytes(KMAX) / 4));
   // A slot with an out-of-range id gets no unit; its h slice is defined as zero.
   if (__any_sync(kFull, s.badmask != 0u)) {
     for (int t = blockIdx.x * kXsWarps + wid; t < p.T; t += gridDim.x * kXsWarps) {
@@ -396,16 +401,9 @@ __global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_3d_batched_xs(GateU
     const uint8_t* su = sg + (size_t)I * nb;
 #pragma unroll 1
     while (tokens) {
-      int tok[NT];
-      int nt = 0;
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        tok[n] = tokens ? __ffs(tokens) - 1 : 0;
-        if (tokens) {
-          tokens &= tokens - 1;
-          ++nt;
-        }
-      }
+      TokenGroup<NT> tg;   // this pass's tokens: the lowest NT of `tokens`
+      tg.take(tokens);
+      const int nt = tg.nt;
       float ag[NT], au[NT];
 #pragma unroll
       for (int n = 0; n < NT; ++n) ag[n] = au[n] = 0.f;
@@ -439,10 +437,11 @@ __global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_3d_batched_xs(GateU
               s_g[d] = ld_scale(sg + b + 32 * D);
               s_u[d] = ld_scale(su + b + 32 * D);
             }
+            uint32_t gm = tg.grp;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
               if (n < nt) {
-                const int xb = tok[n] * nb + b;
+                const int xb = tg.token(n, gm) * nb + b;
                 const uint8_t* act = xs + 64 * xb;
                 const float fx = xf[xb];
                 ag[n] = fmaf(dot_block_h(whg, act, lb) * fx, scg, ag[n]);
@@ -452,14 +451,16 @@ __global__ void __launch_bounds__(kXsThreads, 1) moe_gate_up_3d_batched_xs(GateU
           }
         }
       }
+      uint32_t gm = tg.grp;
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         if (n < nt) {
+          const int t = tg.token(n, gm);
           const float g = warp_sum(ag[n]);
           const float up = warp_sum(au[n]);
-          const uint32_t jt = __shfl_sync(kFull, jm, tok[n]);
+          const uint32_t jt = __shfl_sync(kFull, jm, t);
           const uint16_t hb = f32_to_bf16_rn((g / (1.0f + expf(-g))) * up);
-          if (lane < p.k && ((jt >> lane) & 1u)) p.h[((size_t)tok[n] * p.k + lane) * I + i] = hb;
+          if (lane < p.k && ((jt >> lane) & 1u)) p.h[((size_t)t * p.k + lane) * I + i] = hb;
         }
       }
     }

@@ -55,7 +55,14 @@ constexpr int kTcFirstDecodeWarp = 7;
 constexpr int kTcGuDecodeWarps = 16;
 constexpr int kTcDnDecodeWarps = 8;
 constexpr int kTcGuThreads = (kTcFirstDecodeWarp + kTcGuDecodeWarps) * 32;
+// gate/up decode warps: one per (lane quarter, tensor-memory A stage)
+static_assert(kTcGuDecodeWarps == 4 * kTcGuSA && (kTcGuSA & (kTcGuSA - 1)) == 0, "decode warps");
+// stage lanes split every scale chunk evenly
+static_assert(kTcScaleStages % kTcGuSA == 0, "scale chunk");
 constexpr int kTcDnThreads = (kTcFirstDecodeWarp + kTcDnDecodeWarps) * 32;
+// down decode warps: four lane quarters x kTcDnLanes stage lanes
+constexpr int kTcDnLanes = kTcDnDecodeWarps / 4;
+static_assert(kTcDnLanes == 2 && kTcDnSA % kTcDnLanes == 0, "down decode warps");
 constexpr int kTcPrepThreads = 512;
 constexpr int kTcCombineThreads = 256;
 // warp roles (both projection kernels)
@@ -584,9 +591,10 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t* bar, uint32_t parity, uin
 // moe_tc_gate_up: one persistent CTA per SM over tiles (chunk c, neurons
 // [128 m, 128 m + 128)). Per 64-element stage of H: the raw-code warp brings
 // the tile's 128 gate rows and 128 up rows by TMA (and every 8 stages their
-// 16 scale bytes a row), 16 decode warps turn them into exact bf16 in tensor
-// memory (warp quarter q owns lanes 32q..32q+31 = rows; gate/up x two
-// 32-element halves), the B warp brings the chunk's xg rows, and one thread
+// 16 scale bytes a row), 16 decode warps turn them into exact f16 or bf16 in
+// tensor memory (warp quarter q owns lanes 32q..32q+31 = rows; the four
+// warps of a quarter take every fourth stage, gate and up, so four stages
+// are in decode at once), the B warp brings the chunk's xg rows, and one thread
 // issues 2 x 4 MMAs (gate and up, K = 16 each) into the tile's accumulators.
 // Four epilogue warps turn a finished tile into h while the next one runs.
 // ---------------------------------------------------------------------------
@@ -631,14 +639,14 @@ __global__ void __launch_bounds__(kTcGuThreads, 1) moe_tc_gate_up(const __grid_c
   if (warp == kTcWarpEpi && lane == 0) {
     for (int i = 0; i < R; ++i) {
       mbar_init(&raw_full[i], 1);
-      mbar_init(&raw_empty[i], kTcGuDecodeWarps);
+      mbar_init(&raw_empty[i], 4);   // the four lane quarters' decode warps of the stage
     }
     for (int i = 0; i < kTcSB; ++i) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < kTcGuSA; ++i) {
-      mbar_init(&a_full[i], kTcGuDecodeWarps);
+      mbar_init(&a_full[i], 4);      // the four lane quarters' decode warps of the slot
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < kTcNS; ++i) {
@@ -789,50 +797,59 @@ __global__ void __launch_bounds__(kTcGuThreads, 1) moe_tc_gate_up(const __grid_c
     }
   } else {
     // --------------------------------------------------------------- decode
+    // Warp (quarter q, stage lane j) decodes whole stages for its 32 rows:
+    // the stages gs with gs % kTcGuSA == j (so A slot j), gate and up, both
+    // 32-element halves; four stages are in decode at once.
     const int dw = warp - kTcFirstDecodeWarp;
     const int q = warp & 3;
-    const int up = dw >> 3, half = (dw >> 2) & 1;
-    const int r = 32 * q + lane;                 // row among the tile's gate (or up) rows
-    const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + kTcGuAcol + up * 32 + half * 16;
+    const int j = dw >> 2;
+    const int r = 32 * q + lane;                 // row among the tile's gate (and up) rows
+    const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + kTcGuAcol + j * 64;
     int gs = 0, gc = 0;
     RingPos rr(R);   // the raw ring's slot and phase (no division by R per stage)
-    uint4 scw = make_uint4(0u, 0u, 0u, 0u);
+    uint4 scw[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};   // gate, up
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-      for (int s = 0; s < nS; ++s, ++gs) {
+      for (int s = 0; s < nS; ++s, ++gs, rr.next()) {
         if (s % kTcScaleStages == 0) {
+          // every decode warp reads every scale chunk (its rows' 16 bytes)
           const int slot = gc % kTcNS;
           ok = tc_wait_warp(&sc_full[slot], (gc / kTcNS) & 1, p.err, dead);
           if (!ok) break;
-          scw = *reinterpret_cast<const uint4*>(sc + slot * L.scStage + up * kTcRows * 16 + r * 16);
+          const uint8_t* sr = sc + slot * L.scStage + r * 16;
+          scw[0] = *reinterpret_cast<const uint4*>(sr);
+          scw[1] = *reinterpret_cast<const uint4*>(sr + kTcRows * 16);
           __syncwarp();
           if (lane == 0) mbar_arrive(&sc_empty[slot]);
           ++gc;
         }
-        const int slot = rr.slot;
-        ok = tc_wait_warp(&raw_full[slot], rr.phase, p.err, dead);
+        if ((gs & (kTcGuSA - 1)) != j) continue;
+        ok = tc_wait_warp(&raw_full[rr.slot], rr.phase, p.err, dead);
         if (!ok) break;
-        uint4 cc[2];
-        F::load(raw + slot * L.rawStage + up * kTcRows * RB, r, half, cc);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&raw_empty[slot]);
-        rr.next();
-        const int bi = 2 * (s % kTcScaleStages) + half;   // block within the scale chunk
-        const uint32_t word = bi < 4 ? scw.x : bi < 8 ? scw.y : bi < 12 ? scw.z : scw.w;
-        uint32_t o[16];
-        if constexpr (F16)
-          F::decode_f16(cc, (word >> (8 * (bi & 3))) & 0xFFu, o);
-        else
-          F::decode(cc, (word >> (8 * (bi & 3))) & 0xFFu, o);
-        const int as = gs % kTcGuSA;
-        if (gs >= kTcGuSA) ok = tc_wait_warp(&a_empty[as], ((gs / kTcGuSA) - 1) & 1, p.err, dead);
+        if (gs >= kTcGuSA) ok = tc_wait_warp(&a_empty[j], ((gs / kTcGuSA) - 1) & 1, p.err, dead);
         if (!ok) break;
         tc::fence_after();
-        tc::st16(tcol + as * 64, o);
+        const uint8_t* st = raw + rr.slot * L.rawStage;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {   // block b: gate (b < 2) or up, half b & 1
+          uint4 cc[2];
+          F::load(st + (b >> 1) * kTcRows * RB, r, b & 1, cc);
+          const int bi = 2 * (s % kTcScaleStages) + (b & 1);   // block within the scale chunk
+          const uint4 w4 = scw[b >> 1];
+          const uint32_t word = bi < 4 ? w4.x : bi < 8 ? w4.y : bi < 12 ? w4.z : w4.w;
+          uint32_t o[16];
+          if constexpr (F16)
+            F::decode_f16(cc, (word >> (8 * (bi & 3))) & 0xFFu, o);
+          else
+            F::decode(cc, (word >> (8 * (bi & 3))) & 0xFFu, o);
+          tc::st16(tcol + (b >> 1) * 32 + (b & 1) * 16, o);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[rr.slot]);
         tc::wait_st();
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[as]);
+        if (lane == 0) mbar_arrive(&a_full[j]);
       }
     }
   }
@@ -848,7 +865,7 @@ __global__ void __launch_bounds__(kTcGuThreads, 1) moe_tc_gate_up(const __grid_c
 // moe_tc_down: as moe_tc_gate_up over tiles (chunk c, rows [128 m, 128 m +
 // 128) of y), K = I: per stage 128 W_down rows by TMA, their scales once a
 // tile (a bulk copy of 128 rows of I/32 bytes), 8 decode warps (quarter x
-// half), the chunk's hg rows as B, 4 MMAs into one accumulator; the epilogue
+// every other stage), the chunk's hg rows as B, 4 MMAs into one accumulator; the epilogue
 // writes the pairs' FP32 partial rows yp[p][128 m ...].
 // ---------------------------------------------------------------------------
 template <class F>
@@ -886,14 +903,14 @@ __global__ void __launch_bounds__(kTcDnThreads, 1) moe_tc_down(const __grid_cons
   if (warp == kTcWarpEpi && lane == 0) {
     for (int i = 0; i < R; ++i) {
       mbar_init(&raw_full[i], 1);
-      mbar_init(&raw_empty[i], kTcDnDecodeWarps);
+      mbar_init(&raw_empty[i], 4);   // the four lane quarters' decode warps of the stage
     }
     for (int i = 0; i < kTcSB; ++i) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < kTcDnSA; ++i) {
-      mbar_init(&a_full[i], kTcDnDecodeWarps);
+      mbar_init(&a_full[i], 4);      // the four lane quarters' decode warps of the stage
       mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -1017,10 +1034,12 @@ __global__ void __launch_bounds__(kTcDnThreads, 1) moe_tc_down(const __grid_cons
     }
   } else {
     // --------------------------------------------------------------- decode
+    // Warp (quarter q, stage lane j) decodes whole stages for its 32 rows:
+    // the stages gs with gs % kTcDnLanes == j, both 32-element halves.
     const int dw = warp - kTcFirstDecodeWarp;
-    const int q = warp & 3, half = dw >> 2;
+    const int q = warp & 3, j = dw >> 2;
     const int r = 32 * q + lane;
-    const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + kTcDnAcol + half * 16;
+    const uint32_t tcol = tmem + ((uint32_t)(32 * q) << 16) + kTcDnAcol;
     int gs = 0, lt = 0;
     RingPos rr(R);   // the raw ring's slot and phase (no division by R per stage)
     bool ok = true;
@@ -1029,23 +1048,25 @@ __global__ void __launch_bounds__(kTcDnThreads, 1) moe_tc_down(const __grid_cons
       ok = tc_wait_warp(&sc_full[ss], (lt >> 1) & 1, p.err, dead);
       if (!ok) break;
       const uint8_t* srow = sc + ss * L.scStage + r * nbI;
-      for (int s = 0; s < nS; ++s, ++gs) {
+      for (int s = 0; s < nS; ++s, ++gs, rr.next()) {
+        if ((gs & (kTcDnLanes - 1)) != j) continue;
         const int slot = rr.slot;
         ok = tc_wait_warp(&raw_full[slot], rr.phase, p.err, dead);
         if (!ok) break;
-        uint4 cc[2];
-        F::load(raw + slot * L.rawStage, r, half, cc);
-        const uint32_t sv = srow[2 * s + half];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&raw_empty[slot]);
-        rr.next();
-        uint32_t o[16];
-        F::decode(cc, sv, o);
         const int as = gs % kTcDnSA;
         if (gs >= kTcDnSA) ok = tc_wait_warp(&a_empty[as], ((gs / kTcDnSA) - 1) & 1, p.err, dead);
         if (!ok) break;
         tc::fence_after();
-        tc::st16(tcol + as * 32, o);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint4 cc[2];
+          F::load(raw + slot * L.rawStage, r, half, cc);
+          uint32_t o[16];
+          F::decode(cc, srow[2 * s + half], o);
+          tc::st16(tcol + as * 32 + half * 16, o);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[slot]);
         tc::wait_st();
         tc::fence_before();
         __syncwarp();
